@@ -1,0 +1,444 @@
+#!/usr/bin/env python
+"""Throughput of the groupwise low-bit linear layer on one GB300 (or N replicas).
+
+Workload (default): the Llama-3.1-8B decode linears at M = 1, group 64, bit
+widths 1..7 -- (K, N) = (4096, 6144) qkv, (4096, 4096) o, (4096, 28672)
+gate+up, (14336, 4096) down -- 28 layers.  One step is one call of every
+layer: 28 launches of the qmv kernel over ~0.9 GB of packed weights, scales
+and zeros, more than the 129 MB L2, so every launch reads its weights cold.
+
+  value      algorithmic HBM bytes of a step / device time of a step, GB/s,
+             with all inputs resident in HBM; the step is replayed from a
+             CUDA graph of 28 C-ABI calls.
+  e2e        the same metric with every input copied from pinned host memory
+             and y copied back, through the public Python binding, per step.
+  roofline   the qmv kernel alone: per-layer launch time with CUDA events,
+             L2 flushed before each launch, summed over the 28 layers.
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of output rows.
+
+``--impl reference`` times the CPU oracle instead (the method's plain
+definition; no GPU work).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import synth  # noqa: E402
+
+METRIC = "qmv µs & achieved HBM GB/s (M=1, b=1..7) vs 8 TB/s; qmm TFLOP/s at M=128"
+GROUP = 64
+BITS = tuple(range(1, 8))
+WORKLOAD = "llama3.1-8b decode linears: M=1, g=64, b=1..7, (K,N) in qkv/o/gate_up/down"
+
+
+def layer_list():
+    return [(name, K, N, b) for b in BITS for name, (K, N) in synth.LLAMA_8B.items()]
+
+
+def algorithmic_bytes(M, K, N, bits, group, bias=False, rows=None):
+    """Bytes the method must move: packed codes + fp16 scale and zero + x + y (+ bias)."""
+    n = N if rows is None else rows
+    return n * K * bits // 8 + 4 * n * (K // group) + 2 * M * K + 2 * M * n + (2 * n if bias else 0)
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 0.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (replicas; no collective on the data path).
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+class Dist:
+    def __init__(self, backend):
+        import torch.distributed as dist
+        self.rank, self.world, self.local = dist_env()
+        self.dist = dist if self.world > 1 else None
+        if self.dist is not None:
+            dist.init_process_group(backend=backend)
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, v: float) -> float:
+        if self.dist is None:
+            return v
+        import torch
+        dev = "cuda" if self.dist.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region (nvidia-smi, sampled in the background).
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        rows = [r.split(", ") for r in self.lines if r.count(",") >= 9]
+        if self.bus_id:
+            mine = [r for r in rows if r[1].lower().endswith(self.bus_id.lower()[-12:])]
+            rows = mine or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        idx = rows[0][0]
+        rows = [r for r in rows if r[0] == idx]
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][3]), "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[4]) or 0.0) for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# The CPU oracle on a sample of output rows (reference arm and cpu_baseline).
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """Host inputs for a sample of rows of every layer, packed by the oracle."""
+
+    def __init__(self, rows_per_layer: int, seed: int = 0):
+        import oracle
+        self.o = oracle.Oracle()
+        self.items = []
+        for name, K, N, b in layer_list():
+            key = (b, GROUP)
+            r = np.random.default_rng([seed, K, N, b]).choice(N, rows_per_layer, replace=False)
+            r.sort()
+            x = synth.make_x(seed, 1, K, False, key)
+            codes = synth.make_codes(seed, N, K, b, key)[r]
+            s, z = synth.make_scale_zero(seed, N, K // GROUP, (K, b, GROUP))
+            self.items.append(dict(K=K, b=b, x=x, packed=self.o.pack(codes, b), s=s[r], z=z[r],
+                                   rows=np.arange(r.size), bytes=algorithmic_bytes(
+                                       1, K, N, b, GROUP, rows=r.size)))
+        self.bytes = sum(i["bytes"] for i in self.items)
+
+    def run(self):
+        for i in self.items:
+            self.o.linear_rows(i["x"], i["packed"], i["s"], i["z"], None, i["K"], i["b"], GROUP,
+                               i["rows"])
+
+
+def calibrate_oracle(seconds: float):
+    """Rows per layer such that one pass over all 28 layers takes about ``seconds``."""
+    probe = OracleSample(2)
+    t = time.perf_counter()
+    probe.run()
+    dt = max(time.perf_counter() - t, 1e-6)
+    rows = int(max(1, min(4096, 2 * seconds / dt)))
+    return OracleSample(rows), rows
+
+
+def time_oracle(sample: OracleSample, reps: int = 1):
+    t = time.perf_counter()
+    for _ in range(reps):
+        sample.run()
+    dt = time.perf_counter() - t
+    return sample.bytes * reps / dt / 1e9, dt
+
+
+# ---------------------------------------------------------------------------
+# Arms.
+# ---------------------------------------------------------------------------
+
+def base_config():
+    return {"workload": WORKLOAD, "M": 1, "group": GROUP, "bits": list(BITS),
+            "shapes_KN": {k: list(v) for k, v in synth.LLAMA_8B.items()},
+            "layers_per_step": len(layer_list()), "bias": False,
+            "l2": "inputs larger than L2 (each step streams ~0.9 GB of distinct weights)",
+            "seed": 0}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    total = args.steps + args.warmup
+    per_step = min(5.0, 90.0 / max(total, 1))
+    sample, rows = calibrate_oracle(per_step)
+    for _ in range(args.warmup):
+        sample.run()
+    gbs, dt = time_oracle(sample, args.steps)
+    ms = dt / args.steps * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": base_config(),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} output rows of each of the 28 layers per step"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in sorted((ROOT / "bit_groupwise_weight_gb300" / "csrc").glob("*")):
+        if p.name in ("qmv.cu", "common.cuh"):
+            h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the qmv kernel from the committed ncu summary, if that
+    summary was taken on the current kernel source."""
+    p = ROOT / "profiles" / "qmv_llama8b_decode_traffic.json"
+    if not p.exists():
+        return None
+    d = json.loads(p.read_text())
+    if d.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+    import bit_groupwise_weight_gb300 as lb
+    from bit_groupwise_weight_gb300 import build as lbuild
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = Dist("nccl")
+    lbuild.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(dev)
+
+    # --- inputs: host (pinned) and device copies of every layer -----------------
+    layers = []
+    for name, K, N, b in layer_list():
+        key = (b, GROUP)
+        x = synth.make_x(0, 1, K, False, key)
+        codes = synth.make_codes(0, N, K, b, key)
+        s, z = synth.make_scale_zero(0, N, K // GROUP, (K, b, GROUP))
+        d_codes = torch.from_numpy(codes).to(dev)
+        with torch.cuda.stream(stream):
+            packed = lb.pack_weights(d_codes, b)
+        stream.synchronize()
+        del d_codes
+        t = dict(name=name, K=K, N=N, b=b,
+                 x=torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev),
+                 w=packed,
+                 s=torch.from_numpy(s.view(np.int16)).view(torch.float16).to(dev),
+                 z=torch.from_numpy(z.view(np.int16)).view(torch.float16).to(dev),
+                 y=torch.empty((1, N), dtype=torch.bfloat16, device=dev),
+                 bytes=algorithmic_bytes(1, K, N, b, GROUP))
+        layers.append(t)
+    step_bytes = sum(t["bytes"] for t in layers)
+
+    def call(t, st):
+        lb.linear_ptr(t["x"].data_ptr(), t["w"].data_ptr(), t["s"].data_ptr(), t["z"].data_ptr(),
+                      None, t["y"].data_ptr(), 1, t["K"], t["N"], t["b"], GROUP, st)
+
+    # --- CUDA graph of one step --------------------------------------------------
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for t in layers:           # one eager pass first (module load, first-call setup)
+            call(t, stream.cuda_stream)
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            for t in layers:
+                call(t, stream.cuda_stream)
+    stream.synchronize()
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except AttributeError:
+        bus = None
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            graph.replay()
+    stream.synchronize()
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(bus)
+    clocks.start()
+    time.sleep(0.15)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clk = clocks.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_total = dist.max(ms_total)
+    ms_per_step = ms_total / args.steps
+    value = world * step_bytes * args.steps / (ms_total / 1e3) / 1e9
+
+    # --- per-layer kernel time, cold L2 (roofline of the qmv kernel) -------------
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(int(2 * l2), dtype=torch.uint8, device=dev)
+    per_layer = []
+    reps = 20
+    with torch.cuda.stream(stream):
+        for t in layers:
+            times = []
+            for _ in range(reps):
+                flush.fill_(1)
+                a = torch.cuda.Event(enable_timing=True)
+                c = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                call(t, stream.cuda_stream)
+                c.record(stream)
+                times.append((a, c))
+            stream.synchronize()
+            us = statistics.median(a.elapsed_time(c) * 1e3 for a, c in times)
+            per_layer.append({"layer": t["name"], "bits": t["b"], "K": t["K"], "N": t["N"],
+                              "us": round(us, 3), "GBps": round(t["bytes"] / us / 1e3, 1)})
+    del flush
+    kern_us = sum(p["us"] for p in per_layer)
+    achieved = step_bytes / kern_us / 1e3
+    hbm_peak, tc_peak, peak_kind = measured_peaks()
+
+    # --- e2e: host buffers through the public API --------------------------------
+    e2e_steps = max(1, min(args.steps, 10))
+    host = []
+    for t in layers:
+        host.append({k: t[k].cpu().pin_memory() for k in ("x", "w", "s", "z")}
+                    | {"y": torch.empty((1, t["N"]), dtype=torch.bfloat16).pin_memory()})
+    h2d = sum(sum(h[k].numel() * h[k].element_size() for k in ("x", "w", "s", "z")) for h in host)
+    d2h = sum(h["y"].numel() * 2 for h in host)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for t, h in zip(layers, host):
+                for k in ("x", "w", "s", "z"):
+                    t[k].copy_(h[k], non_blocking=True)
+                lb.linear(t["x"], t["w"], t["s"], t["z"], None, t["b"], GROUP, out=t["y"])
+                h["y"].copy_(t["y"], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = dist.max(e0.elapsed_time(e1)) / e2e_steps
+    e2e_value = world * step_bytes / (e2e_ms / 1e3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": base_config() | {"parallelism": f"replicas{world}" if world > 1 else "single",
+                                   "step_bytes": step_bytes},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": profiled_traffic(),
+                     "kernel": "qmv (all 28 layers; per-launch CUDA-event time, L2 flushed)",
+                     "peak_kind": f"{peak_kind} hbm_gbs (burst copy)"},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": len(layers) * args.steps,
+        "clocks": clk,
+        "layers": per_layer,
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample, rows = calibrate_oracle(args.cpu_seconds)
+        gbs, _ = time_oracle(sample)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{rows} output rows of each of the 28 layers "
+                                          f"(fp64, one thread)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

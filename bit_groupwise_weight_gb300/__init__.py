@@ -1,0 +1,32 @@
+"""bit_groupwise_weight_gb300 -- groupwise low-bit weight-only linear layer on GB300.
+
+Python binding of liblowbit (include/lowbit.h).  This module only marshals
+arguments: it hands device pointers from torch tensors and the current CUDA
+stream to the C ABI.  Every step of the computation runs in the library's
+CUDA kernels; there is no CPU or PyTorch fallback, and every function raises
+if the compiled library is missing.
+
+    packed = pack_weights(codes, bits)            # codes: uint8 [N, K] on cuda
+    y = linear(x, packed, scales, zeros, bias, bits=4, group=64)
+"""
+from __future__ import annotations
+
+from ._abi import (  # noqa: F401
+    LowbitError,
+    PATH_AUTO,
+    PATH_QMM,
+    PATH_QMV,
+    abi,
+    linear,
+    linear_ptr,
+    pack_weights,
+    packed_bytes,
+    select_path,
+    status_string,
+    unpack_weights,
+)
+
+__all__ = [
+    "LowbitError", "PATH_AUTO", "PATH_QMM", "PATH_QMV", "abi", "linear", "linear_ptr",
+    "pack_weights", "packed_bytes", "select_path", "status_string", "unpack_weights",
+]

@@ -1,0 +1,151 @@
+"""ctypes binding of liblowbit: same names as the C ABI in include/lowbit.h.
+
+Argument marshalling only.  Tensors must already live on the GPU with the
+dtypes and layouts the C ABI documents; this module checks dtypes and shapes,
+passes raw pointers and ``torch.cuda.current_stream()``, and turns a non-zero
+status into ``LowbitError``.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+from . import build as _build
+
+LOWBIT_OK, LOWBIT_EINVAL, LOWBIT_EUNSUPPORTED, LOWBIT_ECUDA = 0, 1, 2, 3
+PATH_AUTO, PATH_QMV, PATH_QMM = 0, 1, 2
+
+_lib = None
+
+
+class LowbitError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def _bind(lib):
+    vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.lowbit_status_string.argtypes = [ci]
+    lib.lowbit_status_string.restype = ctypes.c_char_p
+    lib.lowbit_packed_bytes.argtypes = [i64, i64, ci]
+    lib.lowbit_packed_bytes.restype = ctypes.c_size_t
+    lib.lowbit_pack_weights.argtypes = [vp, vp, i64, i64, ci, vp]
+    lib.lowbit_pack_weights.restype = ci
+    lib.lowbit_unpack_weights.argtypes = [vp, vp, i64, i64, ci, vp]
+    lib.lowbit_unpack_weights.restype = ci
+    lib.lowbit_linear.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, vp]
+    lib.lowbit_linear.restype = ci
+    lib.lowbit_linear_ex.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, vp]
+    lib.lowbit_linear_ex.restype = ci
+    lib.lowbit_select_path.argtypes = [i64, i64, i64, ci, ci]
+    lib.lowbit_select_path.restype = ci
+    return lib
+
+
+def library_path() -> Path:
+    return _build.LIB
+
+
+def abi():
+    """The loaded liblowbit (ctypes.CDLL).  Raises ImportError if it was never built."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not path.exists():
+            raise ImportError(
+                f"liblowbit is not built ({path} missing); run bit_groupwise_weight_gb300.build.build()")
+        _lib = _bind(ctypes.CDLL(str(path)))
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return abi().lowbit_status_string(int(status)).decode()
+
+
+def packed_bytes(N: int, K: int, bits: int) -> int:
+    return int(abi().lowbit_packed_bytes(N, K, bits))
+
+
+def select_path(M: int, K: int, N: int, bits: int, group: int) -> int:
+    return int(abi().lowbit_select_path(M, K, N, bits, group))
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != LOWBIT_OK:
+        raise LowbitError(status, what)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def pack_weights(codes: torch.Tensor, bits: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """codes uint8 [N, K] (one code per byte) -> packed uint8 [N, K*bits/8]."""
+    N, K = codes.shape
+    _need(codes, "codes", torch.uint8, (N, K))
+    if out is None:
+        out = torch.empty((N, K * bits // 8), dtype=torch.uint8, device=codes.device)
+    _need(out, "out", torch.uint8, (N, K * bits // 8))
+    _check(abi().lowbit_pack_weights(codes.data_ptr(), out.data_ptr(), N, K, bits,
+                                     _stream(codes.device)), "lowbit_pack_weights")
+    return out
+
+
+def unpack_weights(packed: torch.Tensor, K: int, bits: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    N = packed.shape[0]
+    _need(packed, "packed", torch.uint8, (N, K * bits // 8))
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.uint8, device=packed.device)
+    _need(out, "out", torch.uint8, (N, K))
+    _check(abi().lowbit_unpack_weights(packed.data_ptr(), out.data_ptr(), N, K, bits,
+                                       _stream(packed.device)), "lowbit_unpack_weights")
+    return out
+
+
+def linear(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+           bias: torch.Tensor | None, bits: int, group: int, out: torch.Tensor | None = None,
+           path: int = PATH_AUTO) -> torch.Tensor:
+    """y = x @ W^T + bias with W[n,k] = scales[n,k//g]*q[n,k] + zeros[n,k//g].
+
+    x bf16 [M, K]; packed_w uint8 [N, K*bits/8]; scales, zeros fp16 [N, K/group];
+    bias fp16 [N] or None.  Returns bf16 [M, N] (or writes ``out``).
+    """
+    M, K = x.shape
+    N = packed_w.shape[0]
+    _need(x, "x", torch.bfloat16, (M, K))
+    _need(packed_w, "packed_w", torch.uint8, (N, K * bits // 8))
+    G = K // group if group else 0
+    _need(scales, "scales", torch.float16, (N, G))
+    _need(zeros, "zeros", torch.float16, (N, G))
+    if bias is not None:
+        _need(bias, "bias", torch.float16, (N,))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16, (M, N))
+    _check(abi().lowbit_linear_ex(x.data_ptr(), packed_w.data_ptr(), scales.data_ptr(),
+                                  zeros.data_ptr(), None if bias is None else bias.data_ptr(),
+                                  out.data_ptr(), M, K, N, bits, group, path, _stream(x.device)),
+           "lowbit_linear")
+    return out
+
+
+def linear_ptr(x: int, packed_w: int, scales: int, zeros: int, bias: int | None, y: int,
+               M: int, K: int, N: int, bits: int, group: int, stream: int,
+               path: int = PATH_AUTO) -> None:
+    """The C call on raw device pointers (for CUDA-graph capture and timing loops)."""
+    _check(abi().lowbit_linear_ex(x, packed_w, scales, zeros, bias, y, M, K, N, bits, group, path,
+                                  stream), "lowbit_linear")

@@ -1,0 +1,134 @@
+// api.cu -- the C ABI of liblowbit (declared in include/lowbit.h).
+//
+// Every entry point validates its arguments on the host before it touches
+// CUDA, then enqueues the kernel on the caller's stream.  Nothing here
+// allocates device memory or synchronises.
+#include <atomic>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace {
+
+bool bits_ok(int bits) { return bits >= 1 && bits <= 7; }
+bool group_ok(int g) { return g == 32 || g == 64 || g == 128 || g == 256; }
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Largest sizes accepted: every index the kernels form stays inside int32 for
+// per-row quantities and int64 for whole-buffer offsets.
+constexpr int64_t kMaxDim = (int64_t)1 << 30;
+
+// 0 = unknown, 1 = sm_103, 2 = other.  One slot per device ordinal.
+std::atomic<int> g_device_ok[64];
+
+lowbit_status check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LOWBIT_ECUDA;
+    if (dev < 0 || dev >= 64) return LOWBIT_EUNSUPPORTED;
+    int state = g_device_ok[dev].load(std::memory_order_relaxed);
+    if (state == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return LOWBIT_ECUDA;
+        state = (major == 10 && minor == 3) ? 1 : 2;
+        g_device_ok[dev].store(state, std::memory_order_relaxed);
+    }
+    return state == 1 ? LOWBIT_OK : LOWBIT_EUNSUPPORTED;
+}
+
+lowbit_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LOWBIT_OK : LOWBIT_ECUDA; }
+
+lowbit_status check_pack_args(const void *in, const void *out, int64_t N, int64_t K, int bits,
+                              const void *code_buf) {
+    if (!bits_ok(bits) || N < 0 || K < 0 || N > kMaxDim || K > kMaxDim || K % 8 != 0)
+        return LOWBIT_EINVAL;
+    if (N == 0 || K == 0) return LOWBIT_OK;
+    if (in == nullptr || out == nullptr || !aligned(code_buf, 8)) return LOWBIT_EINVAL;
+    return LOWBIT_OK;
+}
+
+lowbit_status check_linear_args(const uint16_t *x, const uint8_t *w, const uint16_t *s,
+                                const uint16_t *z, const uint16_t *bias, const uint16_t *y,
+                                int64_t M, int64_t K, int64_t N, int bits, int group) {
+    if (!bits_ok(bits) || !group_ok(group)) return LOWBIT_EINVAL;
+    if (M < 0 || N < 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return LOWBIT_EINVAL;
+    if (K % group != 0) return LOWBIT_EINVAL;
+    if (M == 0 || N == 0) return LOWBIT_OK;
+    if (!x || !w || !s || !z || !y) return LOWBIT_EINVAL;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(s, 2) || !aligned(z, 2) || !aligned(y, 2))
+        return LOWBIT_EINVAL;
+    if (bias != nullptr && !aligned(bias, 2)) return LOWBIT_EINVAL;
+    return LOWBIT_OK;
+}
+
+// M at or below which the CUDA-core kernel is faster than the tensor-core one.
+constexpr int64_t kQmvMaxM = kMaxDim;
+
+}  // namespace
+
+extern "C" {
+
+const char *lowbit_status_string(lowbit_status status) {
+    switch (status) {
+        case LOWBIT_OK: return "ok";
+        case LOWBIT_EINVAL: return "invalid argument";
+        case LOWBIT_EUNSUPPORTED: return "unsupported device (needs sm_103 / GB300)";
+        case LOWBIT_ECUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+size_t lowbit_packed_bytes(int64_t N, int64_t K, int bits) {
+    if (!bits_ok(bits) || N < 0 || K < 0 || (K * bits) % 8 != 0) return 0;
+    if (N > kMaxDim || K > kMaxDim) return 0;
+    return (size_t)(N * (K * bits / 8));
+}
+
+lowbit_status lowbit_pack_weights(const uint8_t *codes, uint8_t *packed, int64_t N, int64_t K,
+                                  int bits, lowbit_stream_t stream) {
+    lowbit_status st = check_pack_args(codes, packed, N, K, bits, codes);
+    if (st != LOWBIT_OK || N == 0 || K == 0) return st;
+    if ((st = check_device()) != LOWBIT_OK) return st;
+    return from_cuda(lowbit::launch_pack(codes, packed, N, K, bits, (cudaStream_t)stream));
+}
+
+lowbit_status lowbit_unpack_weights(const uint8_t *packed, uint8_t *codes, int64_t N, int64_t K,
+                                    int bits, lowbit_stream_t stream) {
+    lowbit_status st = check_pack_args(packed, codes, N, K, bits, codes);
+    if (st != LOWBIT_OK || N == 0 || K == 0) return st;
+    if ((st = check_device()) != LOWBIT_OK) return st;
+    return from_cuda(lowbit::launch_unpack(packed, codes, N, K, bits, (cudaStream_t)stream));
+}
+
+lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int group) {
+    if (!bits_ok(bits) || !group_ok(group) || M < 0 || N < 0 || K <= 0 || K % group != 0 ||
+        M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return LOWBIT_PATH_AUTO;
+    return M <= kQmvMaxM ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
+}
+
+lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *packed_w, const uint16_t *scales,
+                               const uint16_t *zeros, const uint16_t *bias, uint16_t *y,
+                               int64_t M, int64_t K, int64_t N, int bits, int group,
+                               lowbit_path path, lowbit_stream_t stream) {
+    if (path != LOWBIT_PATH_AUTO && path != LOWBIT_PATH_QMV && path != LOWBIT_PATH_QMM)
+        return LOWBIT_EINVAL;
+    lowbit_status st = check_linear_args(x, packed_w, scales, zeros, bias, y, M, K, N, bits, group);
+    if (st != LOWBIT_OK || M == 0 || N == 0) return st;
+    if ((st = check_device()) != LOWBIT_OK) return st;
+    if (path == LOWBIT_PATH_AUTO) path = lowbit_select_path(M, K, N, bits, group);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (path == LOWBIT_PATH_QMV)
+        return from_cuda(lowbit::launch_qmv(x, packed_w, scales, zeros, bias, y, M, K, N, bits, group, s));
+    return from_cuda(lowbit::launch_qmm(x, packed_w, scales, zeros, bias, y, M, K, N, bits, group, s));
+}
+
+lowbit_status lowbit_linear(const uint16_t *x, const uint8_t *packed_w, const uint16_t *scales,
+                            const uint16_t *zeros, const uint16_t *bias, uint16_t *y, int64_t M,
+                            int64_t K, int64_t N, int bits, int group, lowbit_stream_t stream) {
+    return lowbit_linear_ex(x, packed_w, scales, zeros, bias, y, M, K, N, bits, group,
+                            LOWBIT_PATH_AUTO, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+// common.cuh -- device helpers shared by the liblowbit kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <utility>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "lowbit.h"
+
+namespace lowbit {
+
+// Packed layout: code k of a row sits at bits [k*b, k*b+b) of the row's
+// little-endian bit stream (ao PR #2167, Summary, bullet 2, read LSB-first).
+// 32 consecutive codes therefore fill exactly b 32-bit little-endian words, and
+// a row of K codes (K % 32 == 0) is K/32 such "blocks" of 4*b bytes.
+constexpr int kBlockCodes = 32;
+
+// Code j (0..31) of a 32-code block held in BITS little-endian words.  All
+// indices are compile-time constants, so a code that straddles two words
+// becomes one funnel shift and a code inside a word one shift + mask.
+template <int BITS, int J>
+__device__ __forceinline__ uint32_t block_code(const uint32_t (&w)[BITS]) {
+    constexpr int bit = J * BITS;
+    constexpr int wi = bit / 32;
+    constexpr int off = bit % 32;
+    constexpr uint32_t mask = (1u << BITS) - 1u;
+    if constexpr (off + BITS <= 32) {
+        return (w[wi] >> off) & mask;
+    } else {
+        return __funnelshift_r(w[wi], w[wi + 1], off) & mask;
+    }
+}
+
+// Exact small-integer -> fp32: the bit pattern 0x4B000000 | q is 2^23 + q for
+// q < 2^23, so one OR and one subtraction replace an int->float conversion.
+__device__ __forceinline__ float code_to_float(uint32_t q) {
+    return __uint_as_float(0x4B000000u | q) - 8388608.0f;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ float half_bits_to_float(uint16_t h) {
+    return __half2float(__ushort_as_half(h));
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// 128-bit streaming load that does not allocate in L1 (weights are read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream_v2(const void *p) {
+    uint2 v;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void *p) {
+    uint32_t v;
+    asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Load the BITS words of one 32-code block starting at a 4*BITS-byte aligned
+// address, with the widest loads that alignment allows.
+template <int BITS>
+__device__ __forceinline__ void load_block(const uint8_t *p, uint32_t (&w)[BITS]) {
+    if constexpr (BITS == 4) {
+        uint4 v = ld_stream_v4(p);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (BITS == 2 || BITS == 6) {
+#pragma unroll
+        for (int i = 0; i < BITS / 2; ++i) {
+            uint2 v = ld_stream_v2(p + 8 * i);
+            w[2 * i] = v.x; w[2 * i + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < BITS; ++i) w[i] = ld_stream_u32(p + 4 * i);
+    }
+}
+
+}  // namespace lowbit
+
+// Launchers implemented in the .cu files (host side, no argument checks: the
+// C ABI in api.cu validates everything first).
+namespace lowbit {
+cudaError_t launch_pack(const uint8_t *codes, uint8_t *packed, int64_t N, int64_t K, int bits,
+                        cudaStream_t stream);
+cudaError_t launch_unpack(const uint8_t *packed, uint8_t *codes, int64_t N, int64_t K, int bits,
+                          cudaStream_t stream);
+cudaError_t launch_qmv(const uint16_t *x, const uint8_t *w, const uint16_t *scales,
+                       const uint16_t *zeros, const uint16_t *bias, uint16_t *y, int64_t M,
+                       int64_t K, int64_t N, int bits, int group, cudaStream_t stream);
+cudaError_t launch_qmm(const uint16_t *x, const uint8_t *w, const uint16_t *scales,
+                       const uint16_t *zeros, const uint16_t *bias, uint16_t *y, int64_t M,
+                       int64_t K, int64_t N, int bits, int group, cudaStream_t stream);
+}  // namespace lowbit

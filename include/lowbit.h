@@ -1,0 +1,149 @@
+/*
+ * lowbit.h -- C ABI of liblowbit, a GB300 (sm_103a) library for the
+ * weight-only, groupwise, asymmetric low-bit linear layer
+ *
+ *     y[m,n] = sum_k x[m,k] * W[n,k] + bias[n],
+ *     W[n,k] = scale[n, k/g] * q[n,k] + zero[n, k/g],
+ *
+ * with q an unsigned b-bit code, b = 1..7, and group size g in {32,64,128,256}.
+ *
+ * Sources (web pages about low-bit weights in torchao / torchchat):
+ *   - torchchat PR #1415 "Add torchao mps ops": the scheme quantises only the
+ *     weights, groupwise, with bit width 1..7 and group size 32..256;
+ *     activations stay floating point.
+ *   - ao PR #2167 "metal lowbit kernels: qmv_fast optimization", Summary:
+ *     bullet 1 -- scales and zeros are N x num_groups; bullet 2 -- the codes
+ *     are stored contiguously, continuing into the next byte once the current
+ *     byte is full; bullet 3 -- a fast matrix-vector kernel (qmv) for decode.
+ *     A reviewer on the same page asks whether it carries over to gemm (qmm).
+ *   - ao issue #3446 "Revamp int4 MPS support in torchao": bias support, and
+ *     the per-bit-width packing op `_pack_weight_{n}bit`.
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     keeps no pointer after a call returns and allocates no device memory.
+ *   - Calls only enqueue work on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and return without synchronising.  A launch error is
+ *     reported as LOWBIT_ECUDA; an error in the kernel itself surfaces at the
+ *     caller's next synchronisation, as for any CUDA kernel.
+ *   - Arguments are checked on the host before anything is launched; a call
+ *     that returns anything but LOWBIT_OK has launched nothing.
+ *   - 16-bit floats are passed as their bit patterns (uint16_t): bf16 for x and
+ *     y, IEEE binary16 (fp16) for scales, zeros and bias.
+ *   - The library holds no global handle; calls from several host threads are
+ *     safe as long as they do not write the same output buffer.
+ *
+ * Packed layout (ao PR #2167, Summary, bullet 2, read LSB-first): row n of the
+ * packed matrix is a byte string of K*b/8 bytes; code k of that row occupies
+ * bits [k*b, k*b+b) of the row's little-endian bit stream, where stream bit j
+ * is bit (j % 8) of byte (j / 8) and bit 0 of the code comes first.  A code
+ * that does not fit in the current byte continues in the next one.  Rows are
+ * stored one after another, so the matrix is [N, K*b/8] row-major.
+ */
+#ifndef LOWBIT_H
+#define LOWBIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define LOWBIT_API __attribute__((visibility("default")))
+#else
+#define LOWBIT_API
+#endif
+
+/* A cudaStream_t (struct CUstream_st *) without pulling in the CUDA headers. */
+typedef struct CUstream_st *lowbit_stream_t;
+
+typedef enum {
+    LOWBIT_OK = 0,
+    LOWBIT_EINVAL = 1,       /* an argument is out of range, null or misaligned   */
+    LOWBIT_EUNSUPPORTED = 2, /* the current device is not an sm_103 (GB300) GPU   */
+    LOWBIT_ECUDA = 3         /* a CUDA runtime call or a kernel launch failed     */
+} lowbit_status;
+
+/* Which kernel lowbit_linear_ex runs. */
+typedef enum {
+    LOWBIT_PATH_AUTO = 0,    /* what lowbit_linear picks (see lowbit_select_path)  */
+    LOWBIT_PATH_QMV = 1,     /* CUDA-core matrix-vector kernel, any M (in chunks)  */
+    LOWBIT_PATH_QMM = 2      /* tensor-core (tcgen05) matrix-matrix kernel, any M  */
+} lowbit_path;
+
+/* Human-readable name of a status code.  Never NULL. */
+LOWBIT_API const char *lowbit_status_string(lowbit_status status);
+
+/* Bytes of a packed [N, K] matrix of b-bit codes: N * K * bits / 8.
+ * Returns 0 when bits is not in 1..7, N or K is negative, or K*bits is not a
+ * multiple of 8 (ao PR #2167, Summary, bullet 2: rows are contiguous bit
+ * streams, so a row only ends on a byte boundary when K*b % 8 == 0). */
+LOWBIT_API size_t lowbit_packed_bytes(int64_t N, int64_t K, int bits);
+
+/* Pack one-code-per-byte codes into the contiguous b-bit layout
+ * (ao PR #2167, Summary, bullet 2; the `_pack_weight_{n}bit` op of
+ * ao issue #3446, one function here for every bit width).
+ *   codes   [N, K] uint8, row-major, device, 8-byte aligned.  Only the low
+ *           `bits` bits of each byte are used; higher bits are ignored.
+ *   packed  [N, K*bits/8] uint8, row-major, device, written in full.
+ *   N >= 0, K >= 0 with K % 8 == 0, bits in 1..7.
+ * Errors: LOWBIT_EINVAL for a bad size, bit width, null pointer (when the
+ * matrix is not empty) or misaligned `codes`; LOWBIT_EUNSUPPORTED on a device
+ * that is not sm_103; LOWBIT_ECUDA when the launch fails.  N == 0 or K == 0
+ * is a valid empty call that launches nothing. */
+LOWBIT_API lowbit_status lowbit_pack_weights(const uint8_t *codes, uint8_t *packed,
+                                  int64_t N, int64_t K, int bits, lowbit_stream_t stream);
+
+/* Inverse of lowbit_pack_weights: one code per output byte (0 .. 2^bits-1).
+ * Same layouts, sizes, alignment and errors as lowbit_pack_weights, with
+ * `codes` the output (8-byte aligned). */
+LOWBIT_API lowbit_status lowbit_unpack_weights(const uint8_t *packed, uint8_t *codes,
+                                    int64_t N, int64_t K, int bits, lowbit_stream_t stream);
+
+/* The quantised linear layer (torchchat PR #1415; ao PR #2167 Summary
+ * bullets 1-3; bias per ao issue #3446):
+ *     y[m,n] = bf16_rn( sum_k x[m,k] * (scale[n,k/g]*q[n,k] + zero[n,k/g]) + bias[n] )
+ * accumulated in fp32.
+ *   x        [M, K] bf16, row-major, device, 16-byte aligned.
+ *   packed_w [N, K*bits/8] uint8 in the packed layout above, 16-byte aligned.
+ *   scales   [N, K/group] fp16, row-major, device, 2-byte aligned.
+ *   zeros    [N, K/group] fp16, row-major, device, 2-byte aligned.  The zero
+ *            is an additive offset: W = scale*q + zero.
+ *   bias     [N] fp16 or NULL (no bias), 2-byte aligned.
+ *   y        [M, N] bf16, row-major, device, 2-byte aligned; written in full.
+ *            y must not overlap any input.
+ *   M >= 0, N >= 0, K > 0, group in {32, 64, 128, 256}, K % group == 0,
+ *   bits in 1..7.  M == 0 or N == 0 is a valid empty call.
+ * The kernel is picked by lowbit_select_path.
+ * Errors: LOWBIT_EINVAL for a bad size, bit width, group, null pointer or
+ * misaligned pointer; LOWBIT_EUNSUPPORTED on a device that is not sm_103;
+ * LOWBIT_ECUDA when a launch fails. */
+LOWBIT_API lowbit_status lowbit_linear(const uint16_t *x, const uint8_t *packed_w,
+                            const uint16_t *scales, const uint16_t *zeros,
+                            const uint16_t *bias, uint16_t *y,
+                            int64_t M, int64_t K, int64_t N, int bits, int group,
+                            lowbit_stream_t stream);
+
+/* lowbit_linear with the kernel chosen by the caller (both kernels are
+ * correct for every M; this is how each is tested and timed on its own).
+ * Same arguments and errors as lowbit_linear, plus LOWBIT_EINVAL for an
+ * unknown `path`. */
+LOWBIT_API lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *packed_w,
+                               const uint16_t *scales, const uint16_t *zeros,
+                               const uint16_t *bias, uint16_t *y,
+                               int64_t M, int64_t K, int64_t N, int bits, int group,
+                               lowbit_path path, lowbit_stream_t stream);
+
+/* The kernel lowbit_linear runs for this problem: LOWBIT_PATH_QMV for small M
+ * (decode), LOWBIT_PATH_QMM above the measured crossover.  Host-only; never
+ * touches the GPU.  Returns LOWBIT_PATH_AUTO for arguments lowbit_linear
+ * would reject. */
+LOWBIT_API lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int group);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOWBIT_H */

@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must build, load, and export every function include/lowbit.h
+declares; argument validation and path selection are host logic and are
+checked here without touching CUDA (every call below is rejected before the
+library makes its first CUDA call, or is pure arithmetic).
+"""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import bit_groupwise_weight_gb300 as lb
+from bit_groupwise_weight_gb300 import build as lbuild
+
+ROOT = Path(__file__).resolve().parent.parent
+EINVAL = 1
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lbuild.build()
+    return lb.abi()
+
+
+def declared_functions():
+    text = "\n".join(p.read_text() for p in sorted((ROOT / "include").glob("*.h")))
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"LOWBIT_API\s+[\w\s\*]*?\b(lowbit_\w+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for fn in ("lowbit_pack_weights", "lowbit_linear", "lowbit_unpack_weights",
+               "lowbit_packed_bytes", "lowbit_status_string", "lowbit_linear_ex",
+               "lowbit_select_path"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(str(lbuild.LIB))
+    for name in declared_functions():
+        assert hasattr(raw, name), f"{name} declared in include/ but not exported"
+
+
+def test_packed_bytes(lib):
+    assert lb.packed_bytes(4096, 4096, 4) == 4096 * 2048
+    assert lb.packed_bytes(3, 8, 3) == 9
+    assert lb.packed_bytes(28672, 4096, 7) == 28672 * 4096 * 7 // 8
+    assert lb.packed_bytes(1, 12, 3) == 0        # 36 bits: not whole bytes
+    assert lb.packed_bytes(1, 32, 0) == 0
+    assert lb.packed_bytes(1, 32, 8) == 0
+    assert lb.packed_bytes(-1, 32, 4) == 0
+    assert lb.packed_bytes(0, 32, 4) == 0
+
+
+def test_status_strings(lib):
+    for s in range(4):
+        assert lb.status_string(s)
+    assert "invalid" in lb.status_string(1)
+    assert lb.status_string(99) == "unknown status"
+
+
+def test_select_path(lib):
+    assert lb.select_path(1, 4096, 4096, 4, 64) == lb.PATH_QMV
+    assert lb.select_path(0, 4096, 4096, 4, 64) == lb.PATH_QMV
+    for bad in ((1, 4096, 4096, 0, 64), (1, 4096, 4096, 8, 64), (1, 4096, 4096, 4, 48),
+                (1, 4000, 4096, 4, 64), (1, 0, 4096, 4, 64), (-1, 4096, 4096, 4, 64)):
+        assert lb.select_path(*bad) == lb.PATH_AUTO
+
+
+LINEAR_ARGS = dict(x=16, w=16, s=2, z=2, bias=0, y=2, M=1, K=64, N=8, bits=4, group=32, path=0)
+
+
+def call_linear(lib, **kw):
+    a = dict(LINEAR_ARGS, **kw)
+    bias = a["bias"] or None
+    return lib.lowbit_linear_ex(a["x"] or None, a["w"] or None, a["s"] or None, a["z"] or None,
+                                bias, a["y"] or None, a["M"], a["K"], a["N"], a["bits"],
+                                a["group"], a["path"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(bits=0), dict(bits=8), dict(group=16), dict(group=512), dict(K=80),
+    dict(K=0), dict(M=-1), dict(N=-3), dict(x=0), dict(w=0), dict(s=0), dict(z=0),
+    dict(y=0), dict(x=8), dict(w=24), dict(s=1), dict(z=3), dict(y=5), dict(bias=7),
+    dict(path=3), dict(K=1 << 31),
+])
+def test_linear_rejects_bad_arguments(lib, kw):
+    # The pointer values are fake; every case fails validation before CUDA is touched.
+    assert call_linear(lib, **kw) == EINVAL
+
+
+def test_linear_empty_is_noop(lib):
+    assert call_linear(lib, M=0) == 0
+    assert call_linear(lib, N=0) == 0
+    assert call_linear(lib, M=0, x=0, w=0, s=0, z=0, y=0) == 0
+
+
+@pytest.mark.parametrize("args", [
+    (16, 16, 8, 32, 0), (16, 16, 8, 32, 8), (16, 16, 8, 12, 3), (0, 16, 8, 32, 4),
+    (16, 0, 8, 32, 4), (12, 16, 8, 32, 4), (16, 16, -1, 32, 4),
+])
+def test_pack_rejects_bad_arguments(lib, args):
+    codes, packed, N, K, bits = args
+    assert lib.lowbit_pack_weights(codes or None, packed or None, N, K, bits, None) == EINVAL
+    assert lib.lowbit_unpack_weights(packed or None, codes or None, N, K, bits, None) == EINVAL
+
+
+def test_pack_empty_is_noop(lib):
+    assert lib.lowbit_pack_weights(None, None, 0, 64, 3, None) == 0
+    assert lib.lowbit_unpack_weights(None, None, 5, 0, 3, None) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import bit_groupwise_weight_gb300._abi as abi_mod
+    monkeypatch.setattr(abi_mod, "_lib", None)
+    monkeypatch.setattr(abi_mod, "library_path", lambda: tmp_path / "missing.so")
+    with pytest.raises(ImportError):
+        abi_mod.abi()

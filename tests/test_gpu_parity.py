@@ -1,0 +1,195 @@
+"""GPU parity: liblowbit's CUDA kernels against the fp64 CPU oracle.
+
+Packing and unpacking must be bit-exact.  The layer output must meet the
+tolerance in tests/parity.py.  Small cases run the oracle on every output;
+the full Llama-shaped layers run it on sampled output rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import DeviceLayer, check_close, y_to_f64
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU machines too; every test here is gpu-marked
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import bit_groupwise_weight_gb300 as lb  # noqa: E402
+from bit_groupwise_weight_gb300 import build as lbuild  # noqa: E402
+
+lbuild.build()
+ORACLE = oracle.Oracle()
+PATHS = [lb.PATH_QMV]
+
+
+# ---------------------------------------------------------------------------
+# Packing (bit-exact).
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits", range(1, 8))
+@pytest.mark.parametrize("N,K", [(1, 8), (3, 32), (17, 96), (5, 256), (64, 4096), (7, 14336)])
+def test_pack_bit_exact(bits, N, K):
+    r = np.random.default_rng(bits * 1000 + N + K)
+    codes = r.integers(0, 256, size=(N, K), dtype=np.uint8)   # high bits must be ignored
+    got = lb.pack_weights(torch.from_numpy(codes).cuda(), bits).cpu().numpy()
+    assert np.array_equal(got, ORACLE.pack(codes, bits))
+
+
+@pytest.mark.parametrize("bits", range(1, 8))
+@pytest.mark.parametrize("N,K", [(1, 8), (17, 96), (64, 4096)])
+def test_unpack_bit_exact(bits, N, K):
+    r = np.random.default_rng(bits * 7 + N)
+    packed = r.integers(0, 256, size=(N, K * bits // 8), dtype=np.uint8)
+    got = lb.unpack_weights(torch.from_numpy(packed).cuda(), K, bits).cpu().numpy()
+    assert np.array_equal(got, ORACLE.unpack(packed, K, bits))
+
+
+def test_pack_full_size_gate_up_7bit():
+    # 8B gate+up at b = 7: 117 M codes -> 103 MB.  Sampled rows against the oracle,
+    # the whole matrix against the kernel's own unpack.
+    N, K, bits = 28672, 4096, 7
+    codes = synth.make_codes(0, N, K, bits)
+    dc = torch.from_numpy(codes).cuda()
+    packed = lb.pack_weights(dc, bits)
+    assert torch.equal(lb.unpack_weights(packed, K, bits), dc)
+    rows = np.random.default_rng(1).choice(N, 64, replace=False)
+    assert np.array_equal(packed[torch.from_numpy(rows).cuda()].cpu().numpy(),
+                          ORACLE.pack(codes[rows], bits))
+
+
+# ---------------------------------------------------------------------------
+# The layer, small shapes: every output against the oracle.
+# ---------------------------------------------------------------------------
+
+def _oracle_y(L):
+    return ORACLE.linear(L.x, ORACLE.pack(L.codes, L.bits), L.scales, L.zeros, L.bias,
+                         L.K, L.bits, L.group)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("bits", range(1, 8))
+@pytest.mark.parametrize("group", [32, 64, 128, 256])
+def test_linear_small_every_bits_group(path, bits, group):
+    L = synth.make_layer(10 + bits, 1, 4 * 256, 131, bits, group, bias=(bits % 2 == 1))
+    d = DeviceLayer(L)
+    check_close(y_to_f64(d.run(path)), _oracle_y(L), f"b={bits} g={group}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 16, 17, 32, 33, 64, 130])
+def test_linear_small_every_m(path, M):
+    L = synth.make_layer(20 + M, M, 640, 257, 5, 64, bias=True, outliers=True)
+    d = DeviceLayer(L)
+    check_close(y_to_f64(d.run(path)), _oracle_y(L), f"M={M}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M,K,N,bits,group", [
+    (1, 32, 1, 3, 32),          # smallest K = g = 32, one output
+    (1, 32, 7, 7, 32),
+    (2, 64, 3, 1, 64),
+    (3, 96, 5, 6, 32),          # K not a multiple of 128
+    (1, 4096 + 32, 33, 4, 32),  # ragged K tail over the CTA's stride
+    (4, 14336, 40, 2, 128),     # long K
+    (1, 256, 1000, 3, 256),     # ragged N
+])
+def test_linear_edge_shapes(path, M, K, N, bits, group):
+    L = synth.make_layer(30 + K + N, M, K, N, bits, group, bias=True)
+    d = DeviceLayer(L)
+    check_close(y_to_f64(d.run(path)), _oracle_y(L), f"{(M, K, N, bits, group)}")
+
+
+def test_linear_single_qmv_full():
+    # K = N = 4096, M = 1, b = 4, g = 64, seed 0: every output.
+    L = synth.make_layer(0, **synth.SINGLE_QMV)
+    d = DeviceLayer(L)
+    check_close(y_to_f64(lb.linear(d.x, d.packed, d.scales, d.zeros, None, 4, 64)), _oracle_y(L))
+
+
+def test_empty_calls_write_nothing():
+    x = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((8, 32), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((8, 1), dtype=torch.float16, device="cuda")
+    y = lb.linear(x, w, s, s, None, 4, 64)
+    assert y.shape == (0, 8)
+    x1 = torch.zeros((1, 64), dtype=torch.bfloat16, device="cuda")
+    w0 = torch.zeros((0, 32), dtype=torch.uint8, device="cuda")
+    s0 = torch.zeros((0, 1), dtype=torch.float16, device="cuda")
+    assert lb.linear(x1, w0, s0, s0, None, 4, 64).shape == (1, 0)
+
+
+def test_misaligned_pointer_is_rejected_on_gpu():
+    L = synth.make_layer(40, 1, 64, 8, 4, 32)
+    d = DeviceLayer(L)
+    xbig = torch.zeros(64 + 1, dtype=torch.bfloat16, device="cuda")
+    xs = xbig[1:].view(1, 64)       # 2-byte offset: not 16-byte aligned
+    with pytest.raises(lb.LowbitError) as e:
+        lb.linear(xs, d.packed, d.scales, d.zeros, None, 4, 32)
+    assert e.value.status == 1
+
+
+def test_repeated_calls_are_deterministic():
+    L = synth.make_layer(41, 1, 4096, 4096, 3, 128)
+    d = DeviceLayer(L)
+    y1 = d.run()
+    y2 = d.run()
+    assert torch.equal(y1, y2)
+
+
+# ---------------------------------------------------------------------------
+# Full-size Llama-shaped layers: sampled rows against the oracle.
+# ---------------------------------------------------------------------------
+
+def _sampled_check(L, rows, path=0, what=""):
+    d = DeviceLayer(L)
+    y = d.run(path)
+    packed_rows = d.packed[torch.from_numpy(rows).cuda()].cpu().numpy()
+    # The oracle packs the sampled rows itself; the device packing is checked bit-exact too.
+    ref_packed = ORACLE.pack(L.codes[rows], L.bits)
+    assert np.array_equal(packed_rows, ref_packed), what
+    ref = ORACLE.linear_rows(L.x, ref_packed, L.scales[rows], L.zeros[rows],
+                             None if L.bias is None else L.bias[rows], L.K, L.bits, L.group,
+                             np.arange(rows.size))
+    check_close(y_to_f64(y)[:, rows], ref, what)
+
+
+def _rows(N, n, seed):
+    r = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, N - 1], r.choice(N, n, replace=False)]))
+
+
+@pytest.mark.parametrize("bits", range(1, 8))
+@pytest.mark.parametrize("name", list(synth.LLAMA_8B))
+def test_llama8b_decode_sweep(bits, name):
+    K, N = synth.LLAMA_8B[name]
+    L = synth.make_layer(0, 1, K, N, bits, 64)
+    _sampled_check(L, _rows(N, 48, bits), what=f"8B {name} b={bits}")
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 6])
+@pytest.mark.parametrize("group", [32, 64, 128, 256])
+@pytest.mark.parametrize("model,name", [("3B", "qkv"), ("3B", "down"), ("1B", "gate_up"), ("1B", "o")])
+def test_llama3b1b_decode(bits, group, model, name):
+    K, N = (synth.LLAMA_3B if model == "3B" else synth.LLAMA_1B)[name]
+    L = synth.make_layer(0, 1, K, N, bits, group)
+    _sampled_check(L, _rows(N, 24, group), what=f"{model} {name} b={bits} g={group}")
+
+
+@pytest.mark.parametrize("M", [2, 4, 8, 16, 32])
+@pytest.mark.parametrize("name", list(synth.LLAMA_8B))
+def test_llama8b_small_batch(M, name):
+    K, N = synth.LLAMA_8B[name]
+    L = synth.make_layer(0, M, K, N, 4, 128, bias=(name == "qkv"))
+    _sampled_check(L, _rows(N, 24, M), what=f"8B {name} M={M}")
+
+
+@pytest.mark.parametrize("M", [128, 2048])
+@pytest.mark.parametrize("bits", [4, 5])
+@pytest.mark.parametrize("name", list(synth.LLAMA_8B))
+def test_llama8b_batched(M, bits, name):
+    K, N = synth.LLAMA_8B[name]
+    L = synth.make_layer(0, M, K, N, bits, 128, bias=True, outliers=True)
+    _sampled_check(L, _rows(N, 6 if M == 2048 else 16, M + bits), what=f"8B {name} M={M} b={bits}")
