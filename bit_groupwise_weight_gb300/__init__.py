@@ -24,9 +24,11 @@ from ._abi import (  # noqa: F401
     select_path,
     status_string,
     unpack_weights,
+    wait_timeouts,
 )
 
 __all__ = [
     "LowbitError", "PATH_AUTO", "PATH_QMM", "PATH_QMV", "abi", "linear", "linear_ptr",
     "pack_weights", "packed_bytes", "select_path", "status_string", "unpack_weights",
+    "wait_timeouts",
 ]

@@ -42,11 +42,17 @@ def _bind(lib):
     lib.lowbit_linear_ex.restype = ci
     lib.lowbit_select_path.argtypes = [i64, i64, i64, ci, ci]
     lib.lowbit_select_path.restype = ci
+    lib.lowbit_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32), ci]
+    lib.lowbit_wait_timeouts.restype = ci
     return lib
 
 
 def library_path() -> Path:
-    return _build.LIB
+    """The in-tree build, or the file named by $LOWBIT_LIBRARY (another build of
+    the same sources, e.g. with different compile-time tuning)."""
+    import os
+    override = os.environ.get("LOWBIT_LIBRARY")
+    return Path(override) if override else _build.LIB
 
 
 def abi():
@@ -71,6 +77,13 @@ def packed_bytes(N: int, K: int, bits: int) -> int:
 
 def select_path(M: int, K: int, N: int, bits: int, group: int) -> int:
     return int(abi().lowbit_select_path(M, K, N, bits, group))
+
+
+def wait_timeouts(reset: bool = False) -> int:
+    """Device-side count of bounded waits that gave up (0 in normal operation)."""
+    n = ctypes.c_uint32(0)
+    _check(abi().lowbit_wait_timeouts(ctypes.byref(n), int(reset)), "lowbit_wait_timeouts")
+    return int(n.value)
 
 
 def _stream(device) -> int:

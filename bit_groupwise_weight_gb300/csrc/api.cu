@@ -131,4 +131,13 @@ lowbit_status lowbit_linear(const uint16_t *x, const uint8_t *packed_w, const ui
                             LOWBIT_PATH_AUTO, stream);
 }
 
+lowbit_status lowbit_wait_timeouts(uint32_t *count, int reset) {
+    if (count == nullptr) return LOWBIT_EINVAL;
+    lowbit_status st = check_device();
+    if (st != LOWBIT_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return LOWBIT_ECUDA;
+    *count = lowbit::qmv_timeouts(reset != 0) + lowbit::qmm_timeouts(reset != 0);
+    return cudaGetLastError() == cudaSuccess ? LOWBIT_OK : LOWBIT_ECUDA;
+}
+
 }  // extern "C"

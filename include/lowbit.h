@@ -142,6 +142,17 @@ LOWBIT_API lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *pack
  * would reject. */
 LOWBIT_API lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int group);
 
+/* Every wait inside the library's kernels (a stage of streamed weights, a
+ * tensor-core completion) is bounded: one that has not completed after about
+ * one second gives up, the kernel finishes without that data (its outputs are
+ * then unspecified) and a device-side counter is incremented.  This returns
+ * the counter for the current device in *count (0 in normal operation) and
+ * clears it when `reset` is non-zero.  Synchronises the current device.
+ * Errors: LOWBIT_EINVAL for a NULL `count`; LOWBIT_EUNSUPPORTED on a device
+ * that is not sm_103; LOWBIT_ECUDA when the synchronisation or the read
+ * fails (for instance after an earlier kernel fault). */
+LOWBIT_API lowbit_status lowbit_wait_timeouts(uint32_t *count, int reset);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,7 +34,7 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for fn in ("lowbit_pack_weights", "lowbit_linear", "lowbit_unpack_weights",
                "lowbit_packed_bytes", "lowbit_status_string", "lowbit_linear_ex",
-               "lowbit_select_path"):
+               "lowbit_select_path", "lowbit_wait_timeouts"):
         assert fn in names
 
 
@@ -111,6 +111,10 @@ def test_pack_rejects_bad_arguments(lib, args):
 def test_pack_empty_is_noop(lib):
     assert lib.lowbit_pack_weights(None, None, 0, 64, 3, None) == 0
     assert lib.lowbit_unpack_weights(None, None, 5, 0, 3, None) == 0
+
+
+def test_wait_timeouts_rejects_null(lib):
+    assert lib.lowbit_wait_timeouts(None, 0) == EINVAL
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

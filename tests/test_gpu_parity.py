@@ -193,3 +193,8 @@ def test_llama8b_batched(M, bits, name):
     K, N = synth.LLAMA_8B[name]
     L = synth.make_layer(0, M, K, N, bits, 128, bias=True, outliers=True)
     _sampled_check(L, _rows(N, 6 if M == 2048 else 16, M + bits), what=f"8B {name} M={M} b={bits}")
+
+
+def test_no_wait_timed_out():
+    # Every bounded wait in the kernels run above completed in time.
+    assert lb.wait_timeouts() == 0
