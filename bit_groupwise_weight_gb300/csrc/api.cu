@@ -63,7 +63,7 @@ lowbit_status check_linear_args(const uint16_t *x, const uint8_t *w, const uint1
 }
 
 // M at or below which the CUDA-core kernel is faster than the tensor-core one.
-constexpr int64_t kQmvMaxM = kMaxDim;
+constexpr int64_t kQmvMaxM = 2;
 
 }  // namespace
 
@@ -105,7 +105,8 @@ lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int gr
     if (!bits_ok(bits) || !group_ok(group) || M < 0 || N < 0 || K <= 0 || K % group != 0 ||
         M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return LOWBIT_PATH_AUTO;
-    return M <= kQmvMaxM ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
+    // The tensor-core kernel needs K % 128 == 0; other shapes stay on the CUDA-core kernel.
+    return (M <= kQmvMaxM || K % 128 != 0) ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
 }
 
 lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *packed_w, const uint16_t *scales,
@@ -121,6 +122,7 @@ lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *packed_w, const
     cudaStream_t s = (cudaStream_t)stream;
     if (path == LOWBIT_PATH_QMV)
         return from_cuda(lowbit::launch_qmv(x, packed_w, scales, zeros, bias, y, M, K, N, bits, group, s));
+    if (!lowbit::qmm_supported(K, x, packed_w)) return LOWBIT_EUNSUPPORTED;
     return from_cuda(lowbit::launch_qmm(x, packed_w, scales, zeros, bias, y, M, K, N, bits, group, s));
 }
 

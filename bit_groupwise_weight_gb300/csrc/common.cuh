@@ -105,6 +105,9 @@ cudaError_t launch_qmv(const uint16_t *x, const uint8_t *w, const uint16_t *scal
 // Bounded waits that gave up, per kernel file (device counters; reading syncs).
 uint32_t qmv_timeouts(bool reset);
 uint32_t qmm_timeouts(bool reset);
+// True when the tensor-core kernel handles this shape (K a multiple of 128,
+// x and packed weights 16-byte aligned).
+bool qmm_supported(int64_t K, const void *x, const void *w);
 cudaError_t launch_qmm(const uint16_t *x, const uint8_t *w, const uint16_t *scales,
                        const uint16_t *zeros, const uint16_t *bias, uint16_t *y, int64_t M,
                        int64_t K, int64_t N, int bits, int group, cudaStream_t stream);

@@ -1,11 +1,517 @@
-// qmm.cu -- tensor-core (tcgen05) quantised matrix-matrix product.  Not built yet.
+// qmm.cu -- quantised matrix-matrix product on the 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory), for batched inputs.
+//
+// Method: y = x W^T + bias with W[n,k] = scale[n,k/g] * q[n,k] + zero[n,k/g]
+// (torchchat PR #1415 "Add torchao mps ops"; ao PR #2167 "metal lowbit
+// kernels: qmv_fast optimization", Summary bullets 1-2, where a reviewer asks
+// whether the matrix-vector kernel carries over to gemm; bias per ao issue
+// #3446).
+//
+// Exact-code formulation.  Rounding each dequantised weight to bf16 before
+// the product costs 2^-9 of |W| per weight, an error that does not shrink with
+// |y| and is too large for near-zero outputs.  Instead the tensor cores
+// multiply the integer codes themselves, which bf16 holds exactly (as 128 + q,
+// q < 128), and the scale and zero are applied per group in fp32:
+//     P_g[n,m] = sum_{k in g} (128 + q[n,k]) x[m,k]       (tensor cores, fp32)
+//     X_g[m]   = sum_{k in g} x[m,k]                      (tensor cores, fp32)
+//     y[m,n]   = sum_g s[n,g] P_g[n,m] + (z[n,g] - 128 s[n,g]) X_g[m] + bias[n]
+// Every product is exact; only fp32 summation rounds.  X_g comes from the
+// last row of each 32-row quarter of the A tile (rows 31, 63, 95, 127), which
+// hold ones instead of codes, so every warp finds X_g in its own lane 31 and a
+// tile covers 124 output rows.
+//
+// Tiling ("swap AB"): the MMA's 128-row A operand is a tile of weight rows
+// (output features n); its B operand is a tile of TN rows of x (TN <= 128,
+// batch rows m).  K advances 128 codes per stage; each group segment (min(g,
+// 128) codes) accumulates into one of up to four TMEM buffers of TN columns.
+//
+// Warp roles (512 threads):
+//   warp 0       TMA producer: per stage one 2D tensor copy of the 128 x 16b
+//                packed-code tile and two 2D copies (64-wide, 128-byte swizzle)
+//                of the x tile, completing on the stage's mbarrier;
+//   warp 1       allocates tensor memory; one lane issues the MMAs
+//                (tcgen05.mma kind::f16, bf16 x bf16 -> fp32) and commits them
+//                to mbarriers that free buffers or hand a segment on;
+//   warps 2..7   unpack codes into bf16 pairs in the 128-byte-swizzled
+//                K-major layout the MMA reads;
+//   warps 8..15  accumulate: per segment read P_g and X_g from tensor memory,
+//                apply scale and zero in fp32, and at the end add the bias and
+//                store y (two warps per tensor-memory lane quarter).
+// All waits are bounded (about one second) and count a timeout instead of
+// hanging; tensor memory is always released before the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace lowbit {
-uint32_t qmm_timeouts(bool) { return 0; }
-cudaError_t launch_qmm(const uint16_t *, const uint8_t *, const uint16_t *, const uint16_t *,
-                       const uint16_t *, uint16_t *, int64_t, int64_t, int64_t, int, int,
-                       cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int kBM = 128;             // rows of an A tile (MMA M)
+constexpr int kRowsOut = kBM - 4;    // output rows per tile; rows 31, 63, 95, 127 hold ones
+constexpr int kBK = 128;             // codes per K stage
+constexpr int kInStages = 3;         // packed codes + x ring
+constexpr int kAStages = 2;          // code-tile ring
+constexpr int kUnpackWarps = 6;
+constexpr int kAccWarps = 8;
+constexpr int kFirstUnpackWarp = 2;
+constexpr int kFirstAccWarp = kFirstUnpackWarp + kUnpackWarps;    // 8
+constexpr int kThreads = (kFirstAccWarp + kAccWarps) * 32;        // 512
+constexpr int kMaxTmemBufs = 4;
+constexpr uint32_t kAStageBytes = kBM * kBK * 2;                  // two 64-column swizzle atoms
+constexpr uint32_t kBf16Magic = 0x43004300u;                      // bf16 pair (128, 128)
+
+__device__ unsigned int g_qmm_timeouts;
+
+struct QmmParams {
+    const uint16_t *s;
+    const uint16_t *z;
+    const uint16_t *bias;
+    uint16_t *y;
+    int M, N, K, G, log2g, TN, tmem_cols, nbuf, ktiles, lseg_log2, nseg;
+    uint32_t x_stage;       // TN * kBK * 2 bytes (two swizzle atoms of TN rows)
+    uint32_t in_stage;      // x_stage + packed tile, rounded to 1024
+    uint32_t a_off, in_off, xs_off;   // offsets from the 1024-aligned base
+    uint32_t idesc;         // tcgen05 instruction descriptor
+};
+
+// 32 bits of a block's little-endian code stream starting at bit START
+// (negative START: zeros shifted in from below).
+template <int BITS, int START>
+__device__ __forceinline__ uint32_t stream_window(const uint32_t (&w)[BITS]) {
+    if constexpr (START < 0) {
+        return w[0] << (-START);
+    } else {
+        constexpr int wi = START / 32, off = START % 32;
+        if constexpr (off == 0) {
+            return w[wi];
+        } else {
+            const uint32_t hi = (wi + 1 < BITS) ? w[wi + 1 < BITS ? wi + 1 : 0] : 0u;
+            return __funnelshift_r(w[wi], hi, off);
+        }
+    }
 }
+
+// Word I (0..15) of a 32-code block as the bf16 pair (128 + q[2I], 128 + q[2I+1]).
+template <int BITS, int I>
+__device__ __forceinline__ uint32_t code_pair(const uint32_t (&w)[BITS]) {
+    constexpr uint32_t m = (1u << BITS) - 1u;
+    if constexpr (BITS == 4) {
+        // One byte = the pair; byte * (1 + 2^12) puts its high nibble at bit 16.
+        const uint32_t byte = ptx::prmt(w[I / 4], 0u, 0x4440u | (I % 4));
+        return ptx::lop3_and_or(byte * 0x1001u, 0x000F000Fu, kBf16Magic);
+    } else if constexpr (BITS == 2) {
+        const uint32_t byte = ptx::prmt(w[I / 8], 0u, 0x4440u | ((I / 2) % 4));
+        uint32_t v = byte * (1u + (1u << 14));
+        if constexpr (I % 2) v >>= 4;
+        return ptx::lop3_and_or(v, 0x00030003u, kBf16Magic);
+    } else if constexpr (BITS == 1) {
+        const uint32_t byte = ptx::prmt(w[I / 16], 0u, 0x4440u | ((I / 4) % 4));
+        uint32_t v = byte * (1u + (1u << 15));
+        if constexpr (I % 4) v >>= (I % 4) * 2;
+        return ptx::lop3_and_or(v, 0x00010001u, kBf16Magic);
+    } else if constexpr (2 * BITS <= 16 - BITS) {
+        // 3 or 5 bits: the pair's 2b bits, spread by one multiply.
+        const uint32_t c = stream_window<BITS, 2 * I * BITS>(w) & ((1u << (2 * BITS)) - 1u);
+        return ptx::lop3_and_or(c * (1u + (1u << (16 - BITS))), m | (m << 16), kBf16Magic);
+    } else {
+        const uint32_t lo = stream_window<BITS, 2 * I * BITS>(w);
+        const uint32_t hi = stream_window<BITS, (2 * I + 1) * BITS - 16>(w);
+        return ptx::lop3_and_or(hi, m << 16, ptx::lop3_and_or(lo, m, kBf16Magic));
+    }
+}
+
+template <int BITS>
+__device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t (&w)[BITS]) {
+    if constexpr (BITS == 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (BITS == 2 || BITS == 6) {
+#pragma unroll
+        for (int i = 0; i < BITS / 2; ++i) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(p + 8 * i);
+            w[2 * i] = v.x; w[2 * i + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < BITS; ++i) w[i] = reinterpret_cast<const uint32_t *>(p)[i];
+    }
+}
+
+// Byte address of the 16-byte chunk `chunk` (0..15 along K) of row r in a
+// 128 x 128 bf16 tile stored as two 128-byte-swizzled K-major atoms.
+__device__ __forceinline__ uint32_t a_chunk_offset(int r, int chunk) {
+    return (uint32_t)((chunk >> 3) * (kBM * 128) + (r >> 3) * 1024 + (r & 7) * 128 +
+                      (((chunk & 7) ^ (r & 7)) << 4));
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, 1)
+qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+           const QmmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;            // swizzle atoms need 1024-byte alignment
+    uint8_t *smem = smem_raw + (base - raw);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kRowsOut;
+    const int m0 = blockIdx.y * p.TN;
+    constexpr uint32_t kPackedStage = kBM * (kBK * BITS / 8);
+
+    // Barriers (8 bytes each), then the TMEM address.
+    const uint32_t in_full = base, in_empty = in_full + 8 * kInStages;
+    const uint32_t a_full = in_empty + 8 * kInStages, a_empty = a_full + 8 * kAStages;
+    const uint32_t t_full = a_empty + 8 * kAStages, t_empty = t_full + 8 * kMaxTmemBufs;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + (t_empty + 8 * kMaxTmemBufs - base));
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kInStages; ++i) {
+            ptx::mbar_init(in_full + 8 * i, 1);
+            ptx::mbar_init(in_empty + 8 * i, kUnpackWarps + 1);
+        }
+        for (int i = 0; i < kAStages; ++i) {
+            ptx::mbar_init(a_full + 8 * i, kUnpackWarps);
+            ptx::mbar_init(a_empty + 8 * i, 1);
+        }
+        for (int i = 0; i < kMaxTmemBufs; ++i) {
+            ptx::mbar_init(t_full + 8 * i, 1);
+            ptx::mbar_init(t_empty + 8 * i, kAccWarps);
+        }
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+        ptx::tmem_relinquish();
+    }
+    // Rows 31, 63, 95, 127 of both A stages: bf16 ones (written once, never overwritten).
+    if (warp >= kFirstUnpackWarp && warp < kFirstAccWarp) {
+        const int t = (warp - kFirstUnpackWarp) * 32 + lane;    // (stage, quarter, chunk)
+        if (t < kAStages * 4 * 16) {
+            uint8_t *a_st = smem + p.a_off + (t >> 6) * kAStageBytes;
+            *reinterpret_cast<uint4 *>(a_st + a_chunk_offset(((t >> 4) & 3) * 32 + 31, t & 15)) =
+                make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        }
+        ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const uint32_t a_base = base + p.a_off;
+    const uint32_t in_base = base + p.in_off;
+    const int lseg = 1 << p.lseg_log2;           // codes per segment (min(g, 128))
+    const int sps = kBK >> p.lseg_log2;          // segments per stage
+
+    if (warp == 0) {
+        // ---------------- TMA producer.
+        if (lane == 0) {
+            const uint64_t pol = ptx::policy_evict_first();
+            int issued = 0;
+            for (int kt = 0; kt < p.ktiles; ++kt, ++issued) {
+                const int st = kt % kInStages;
+                if (kt >= kInStages &&
+                    !ptx::mbar_wait(in_empty + 8 * st, ((kt / kInStages) - 1) & 1, &g_qmm_timeouts))
+                    break;
+                const uint32_t bar = in_full + 8 * st;
+                const uint32_t xs = in_base + st * p.in_stage;
+                ptx::mbar_arrive_expect_tx(bar, p.x_stage + kPackedStage);
+                ptx::tma_load_2d(xs, &xmap, kt * kBK, m0, bar);
+                ptx::tma_load_2d(xs + p.x_stage / 2, &xmap, kt * kBK + 64, m0, bar);
+                ptx::tma_load_2d_hint(xs + p.x_stage, &wmap, kt * (kBK * BITS / 8), n0, bar, pol);
+            }
+            for (int i = max(0, issued - kInStages); i < issued; ++i)
+                if (!ptx::mbar_wait(in_full + 8 * (i % kInStages), (i / kInStages) & 1, &g_qmm_timeouts))
+                    break;
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer.
+        if (lane == 0) {
+            bool ok = true;
+            for (int kt = 0; kt < p.ktiles && ok; ++kt) {
+                const int st = kt % kInStages, as = kt % kAStages;
+                ok = ptx::mbar_wait(in_full + 8 * st, (kt / kInStages) & 1, &g_qmm_timeouts) &&
+                     ptx::mbar_wait(a_full + 8 * as, (kt / kAStages) & 1, &g_qmm_timeouts);
+                if (!ok) break;
+                const uint32_t a_st = a_base + as * kAStageBytes;
+                const uint32_t x_st = in_base + st * p.in_stage;
+                for (int sg = 0; sg < sps && ok; ++sg) {
+                    const int seg = kt * sps + sg;
+                    const int b = seg % p.nbuf;
+                    if (seg >= p.nbuf)
+                        ok = ptx::mbar_wait(t_empty + 8 * b, ((seg / p.nbuf) - 1) & 1, &g_qmm_timeouts);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    const int kk0 = sg * (lseg / 16);
+                    for (int kk = kk0; kk < kk0 + lseg / 16; ++kk) {
+                        const uint32_t atom = kk >> 2, koff = (kk & 3) * 32;
+                        const uint64_t ad = ptx::sw128_desc(a_st + atom * (kBM * 128) + koff);
+                        const uint64_t bd = ptx::sw128_desc(x_st + atom * (p.x_stage / 2) + koff);
+                        ptx::mma_f16(tmem + (uint32_t)(b * p.TN), ad, bd, p.idesc, kk != kk0);
+                    }
+                    ptx::mma_commit(t_full + 8 * b);
+                }
+                ptx::mma_commit(in_empty + 8 * st);
+                ptx::mma_commit(a_empty + 8 * as);
+            }
+        }
+    } else if (warp < kFirstAccWarp) {
+        // ---------------- code unpackers (warps 2..7): 124 rows x 4 blocks per stage.
+        const int ut = (warp - kFirstUnpackWarp) * 32 + lane;    // 0..191
+        bool ok = true;
+        for (int kt = 0; kt < p.ktiles && ok; ++kt) {
+            const int st = kt % kInStages, as = kt % kAStages;
+            ok = ptx::mbar_wait(in_full + 8 * st, (kt / kInStages) & 1, &g_qmm_timeouts);
+            if (ok && kt >= kAStages)
+                ok = ptx::mbar_wait(a_empty + 8 * as, ((kt / kAStages) - 1) & 1, &g_qmm_timeouts);
+            if (!ok) break;
+            const uint8_t *pk = smem + p.in_off + st * p.in_stage + p.x_stage;
+            uint8_t *a_st = smem + p.a_off + as * kAStageBytes;
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                const int task = ut + kUnpackWarps * 32 * i;
+                const int pr = task >> 2, blk = task & 3;     // packed row within the tile
+                if (pr < kRowsOut) {
+                    const int r = pr + pr / 31;               // A row: skip the ones rows
+                    uint32_t w[BITS];
+                    lds_words<BITS>(pk + (pr * (kBK / 32) + blk) * (4 * BITS), w);
+                    uint32_t h[16];
+                    [&]<int... J>(std::integer_sequence<int, J...>) {
+                        ((h[J] = code_pair<BITS, J>(w)), ...);
+                    }(std::make_integer_sequence<int, 16>{});
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(a_st + a_chunk_offset(r, blk * 4 + c)) =
+                            make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                }
+            }
+            ptx::fence_proxy_async_smem();      // generic-proxy stores -> tensor-core reads
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(in_empty + 8 * st);
+                ptx::mbar_arrive(a_full + 8 * as);
+            }
+        }
+    } else {
+        // ---------------- accumulators (warps 8..15).
+        const int q = warp & 3;                          // tensor-memory lane quarter
+        const int h = (warp - kFirstAccWarp) >> 2;       // which half of the 16-column chunks
+        const int n = n0 + q * 31 + lane;                // TMEM lane 32q + lane; lane 31 is a ones row
+        const bool row_ok = lane < 31 && n < p.N;
+        const int nrow = min(n, p.N - 1);
+        // Warp-private slot for lane 31's group sums (32 floats).
+        float *xw = reinterpret_cast<float *>(smem + p.xs_off) + (warp - kFirstAccWarp) * 32;
+        const int nchunk = p.TN / 16;
+        float2 acc[4][8];                                // chunks h, h+2, h+4, h+6
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[c][j] = make_float2(0.f, 0.f);
+        bool ok = true;
+        const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+        for (int seg = 0; seg < p.nseg; ++seg) {
+            const int b = seg % p.nbuf;
+            const int gi = (seg << p.lseg_log2) >> p.log2g;
+            const float sv = half_bits_to_float(__ldg(p.s + (int64_t)nrow * p.G + gi));
+            const float zv = half_bits_to_float(__ldg(p.z + (int64_t)nrow * p.G + gi));
+            const float2 s2 = make_float2(sv, sv);
+            const float zc = fmaf(-128.f, sv, zv);      // zero minus the codes' +128 offset
+            const float2 z2 = make_float2(zc, zc);
+            if (ok) ok = ptx::mbar_wait(t_full + 8 * b, (seg / p.nbuf) & 1, &g_qmm_timeouts);
+            ptx::tc_fence_after();
+            bool released = false;                        // one t_empty arrival per warp per segment
+#pragma unroll
+            for (int c2 = 0; c2 < 4; c2 += 2) {          // two chunks per tensor-memory wait
+                uint32_t v[2][16];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int ch = h + 2 * (c2 + u);
+                    if (ch < nchunk) ptx::tmem_ld16(trow + (uint32_t)(b * p.TN + ch * 16), v[u]);
+                }
+                ptx::tmem_ld_wait();
+                if (!released && (c2 + 2 >= 4 || h + 2 * (c2 + 2) >= nchunk)) {
+                    // Last tensor-memory read of this segment: hand the buffer back.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(t_empty + 8 * b);
+                    released = true;
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int ch = h + 2 * (c2 + u);
+                    if (ch < nchunk) {
+                        if (lane == 31) {
+#pragma unroll
+                            for (int j = 0; j < 16; j += 4)
+                                *reinterpret_cast<uint4 *>(xw + u * 16 + j) =
+                                    make_uint4(v[u][j], v[u][j + 1], v[u][j + 2], v[u][j + 3]);
+                        }
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int ch = h + 2 * (c2 + u);
+                    if (ch < nchunk) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 xg = *reinterpret_cast<const float4 *>(xw + u * 16 + j);
+                            float2 &a0 = acc[c2 + u][j / 2], &a1 = acc[c2 + u][j / 2 + 1];
+                            ptx::ffma2(a0, make_float2(__uint_as_float(v[u][j]), __uint_as_float(v[u][j + 1])), s2, a0);
+                            ptx::ffma2(a1, make_float2(__uint_as_float(v[u][j + 2]), __uint_as_float(v[u][j + 3])), s2, a1);
+                            ptx::ffma2(a0, make_float2(xg.x, xg.y), z2, a0);
+                            ptx::ffma2(a1, make_float2(xg.z, xg.w), z2, a1);
+                        }
+                    }
+                }
+                __syncwarp();                            // xw is reused by the next pair of chunks
+            }
+        }
+        if (ok && row_ok) {
+            const float bias = p.bias != nullptr ? half_bits_to_float(p.bias[n]) : 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int ch = h + 2 * c;
+                if (ch < nchunk) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = m0 + ch * 16 + j;
+                        const float v = (j & 1) ? acc[c][j / 2].y : acc[c][j / 2].x;
+                        if (m < p.M) p.y[(int64_t)m * p.N + n] = float_to_bf16_bits(v + bias);
+                    }
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) ptx::tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load(std::memory_order_acquire);
+    if (f == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f, std::memory_order_release);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+std::atomic<int> g_smem_attr_set[8];
+
+template <int BITS>
+cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
+                        const uint16_t *bias, uint16_t *y, int M, int K, int N, int group,
+                        cudaStream_t stream) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    QmmParams q{};
+    q.s = s; q.z = z; q.bias = bias; q.y = y;
+    q.M = M; q.N = N; q.K = K; q.G = K / group; q.log2g = __builtin_ctz((unsigned)group);
+    q.TN = M >= 128 ? 128 : ((M + 15) / 16) * 16;
+    q.nbuf = std::min(kMaxTmemBufs, 512 / q.TN);
+    const int cols = q.nbuf * q.TN;
+    q.tmem_cols = cols <= 32 ? 32 : (cols <= 64 ? 64 : (cols <= 128 ? 128 : (cols <= 256 ? 256 : 512)));
+    q.ktiles = K / kBK;
+    q.lseg_log2 = std::min(q.log2g, 7);
+    q.nseg = K >> q.lseg_log2;
+    q.x_stage = (uint32_t)q.TN * kBK * 2u;
+    const uint32_t packed = kBM * (kBK * BITS / 8);
+    q.in_stage = (q.x_stage + packed + 1023u) & ~1023u;
+    q.xs_off = 256;                                   // 8 warps x 32 fp32 group sums
+    q.a_off = 2048;
+    q.in_off = q.a_off + kAStages * kAStageBytes;
+    const uint32_t smem = 1024u + q.in_off + kInStages * q.in_stage;   // + alignment slack
+    q.idesc = (1u << 4)                        // accumulate in fp32
+            | (1u << 7) | (1u << 10)           // A and B are bf16
+            | ((uint32_t)(q.TN >> 3) << 17)    // N
+            | ((uint32_t)(kBM >> 4) << 24);    // M = 128
+
+    CUtensorMap xmap, wmap;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)q.TN};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t row_bytes = (cuuint64_t)K * BITS / 8;
+        const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {row_bytes};
+        const cuuint32_t box[2] = {(cuuint32_t)(kBK * BITS / 8), (cuuint32_t)kBM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    if (g_smem_attr_set[BITS].load(std::memory_order_relaxed) == 0) {
+        cudaFuncSetAttribute(reinterpret_cast<const void *>(&qmm_kernel<BITS>),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        g_smem_attr_set[BITS].store(1, std::memory_order_relaxed);
+    }
+    const dim3 grid((N + kRowsOut - 1) / kRowsOut, (M + q.TN - 1) / q.TN);
+    qmm_kernel<BITS><<<grid, kThreads, smem, stream>>>(xmap, wmap, q);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool qmm_supported(int64_t K, const void *x, const void *w) {
+    return K % kBK == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
+           (reinterpret_cast<uintptr_t>(w) & 15u) == 0;
+}
+
+uint32_t qmm_timeouts(bool reset) {
+    unsigned int v = 0;
+    cudaMemcpyFromSymbol(&v, g_qmm_timeouts, sizeof(v));
+    if (reset) {
+        const unsigned int zero = 0;
+        cudaMemcpyToSymbol(g_qmm_timeouts, &zero, sizeof(zero));
+    }
+    return v;
+}
+
+cudaError_t launch_qmm(const uint16_t *x, const uint8_t *w, const uint16_t *scales,
+                       const uint16_t *zeros, const uint16_t *bias, uint16_t *y, int64_t M,
+                       int64_t K, int64_t N, int bits, int group, cudaStream_t stream) {
+    const int k = (int)K, n = (int)N;
+    // Grid y is limited to 65535 tiles of up to 128 rows: chunk very large M.
+    for (int64_t m0 = 0; m0 < M; m0 += (int64_t)65535 * 128) {
+        const int mc = (int)std::min<int64_t>(M - m0, (int64_t)65535 * 128);
+        const uint16_t *xc = x + m0 * K;
+        uint16_t *yc = y + m0 * N;
+        cudaError_t e;
+        switch (bits) {
+            case 1: e = launch_bits<1>(xc, w, scales, zeros, bias, yc, mc, k, n, group, stream); break;
+            case 2: e = launch_bits<2>(xc, w, scales, zeros, bias, yc, mc, k, n, group, stream); break;
+            case 3: e = launch_bits<3>(xc, w, scales, zeros, bias, yc, mc, k, n, group, stream); break;
+            case 4: e = launch_bits<4>(xc, w, scales, zeros, bias, yc, mc, k, n, group, stream); break;
+            case 5: e = launch_bits<5>(xc, w, scales, zeros, bias, yc, mc, k, n, group, stream); break;
+            case 6: e = launch_bits<6>(xc, w, scales, zeros, bias, yc, mc, k, n, group, stream); break;
+            case 7: e = launch_bits<7>(xc, w, scales, zeros, bias, yc, mc, k, n, group, stream); break;
+            default: return cudaErrorInvalidValue;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 }  // namespace lowbit

@@ -129,7 +129,8 @@ LOWBIT_API lowbit_status lowbit_linear(const uint16_t *x, const uint8_t *packed_
 /* lowbit_linear with the kernel chosen by the caller (both kernels are
  * correct for every M; this is how each is tested and timed on its own).
  * Same arguments and errors as lowbit_linear, plus LOWBIT_EINVAL for an
- * unknown `path`. */
+ * unknown `path` and LOWBIT_EUNSUPPORTED when LOWBIT_PATH_QMM is asked for a
+ * shape the tensor-core kernel does not take (K not a multiple of 128). */
 LOWBIT_API lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *packed_w,
                                const uint16_t *scales, const uint16_t *zeros,
                                const uint16_t *bias, uint16_t *y,
@@ -137,9 +138,9 @@ LOWBIT_API lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *pack
                                lowbit_path path, lowbit_stream_t stream);
 
 /* The kernel lowbit_linear runs for this problem: LOWBIT_PATH_QMV for small M
- * (decode), LOWBIT_PATH_QMM above the measured crossover.  Host-only; never
- * touches the GPU.  Returns LOWBIT_PATH_AUTO for arguments lowbit_linear
- * would reject. */
+ * (decode) and for K not a multiple of 128, LOWBIT_PATH_QMM above the
+ * measured crossover.  Host-only; never touches the GPU.  Returns
+ * LOWBIT_PATH_AUTO for arguments lowbit_linear would reject. */
 LOWBIT_API lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int group);
 
 /* Every wait inside the library's kernels (a stage of streamed weights, a

@@ -22,7 +22,8 @@ from bit_groupwise_weight_gb300 import build as lbuild  # noqa: E402
 
 lbuild.build()
 ORACLE = oracle.Oracle()
-PATHS = [lb.PATH_QMV]
+PATHS = [lb.PATH_QMV, lb.PATH_QMM]
+PATH_IDS = {lb.PATH_QMV: "qmv", lb.PATH_QMM: "qmm"}
 
 
 # ---------------------------------------------------------------------------
@@ -69,7 +70,7 @@ def _oracle_y(L):
                          L.K, L.bits, L.group)
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PATH_IDS[p])
 @pytest.mark.parametrize("bits", range(1, 8))
 @pytest.mark.parametrize("group", [32, 64, 128, 256])
 def test_linear_small_every_bits_group(path, bits, group):
@@ -78,7 +79,7 @@ def test_linear_small_every_bits_group(path, bits, group):
     check_close(y_to_f64(d.run(path)), _oracle_y(L), f"b={bits} g={group}")
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PATH_IDS[p])
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 16, 17, 32, 33, 64, 130])
 def test_linear_small_every_m(path, M):
     L = synth.make_layer(20 + M, M, 640, 257, 5, 64, bias=True, outliers=True)
@@ -86,7 +87,7 @@ def test_linear_small_every_m(path, M):
     check_close(y_to_f64(d.run(path)), _oracle_y(L), f"M={M}")
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PATH_IDS[p])
 @pytest.mark.parametrize("M,K,N,bits,group", [
     (1, 32, 1, 3, 32),          # smallest K = g = 32, one output
     (1, 32, 7, 7, 32),
@@ -99,6 +100,12 @@ def test_linear_small_every_m(path, M):
 def test_linear_edge_shapes(path, M, K, N, bits, group):
     L = synth.make_layer(30 + K + N, M, K, N, bits, group, bias=True)
     d = DeviceLayer(L)
+    if path == lb.PATH_QMM and K % 128 != 0:
+        # The tensor-core kernel takes K in steps of 128 codes; it refuses other shapes.
+        with pytest.raises(lb.LowbitError) as e:
+            d.run(path)
+        assert e.value.status == 2
+        return
     check_close(y_to_f64(d.run(path)), _oracle_y(L), f"{(M, K, N, bits, group)}")
 
 
@@ -178,12 +185,13 @@ def test_llama3b1b_decode(bits, group, model, name):
     _sampled_check(L, _rows(N, 24, group), what=f"{model} {name} b={bits} g={group}")
 
 
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PATH_IDS[p])
 @pytest.mark.parametrize("M", [2, 4, 8, 16, 32])
 @pytest.mark.parametrize("name", list(synth.LLAMA_8B))
-def test_llama8b_small_batch(M, name):
+def test_llama8b_small_batch(path, M, name):
     K, N = synth.LLAMA_8B[name]
     L = synth.make_layer(0, M, K, N, 4, 128, bias=(name == "qkv"))
-    _sampled_check(L, _rows(N, 24, M), what=f"8B {name} M={M}")
+    _sampled_check(L, _rows(N, 24, M), path=path, what=f"8B {name} M={M}")
 
 
 @pytest.mark.parametrize("M", [128, 2048])
@@ -193,6 +201,19 @@ def test_llama8b_batched(M, bits, name):
     K, N = synth.LLAMA_8B[name]
     L = synth.make_layer(0, M, K, N, bits, 128, bias=True, outliers=True)
     _sampled_check(L, _rows(N, 6 if M == 2048 else 16, M + bits), what=f"8B {name} M={M} b={bits}")
+
+
+@pytest.mark.parametrize("bits", range(1, 8))
+def test_qmm_every_bits_full_tiles(bits):
+    # Several 128-row tiles, several K stages, M spanning two 128-row x tiles plus a tail.
+    L = synth.make_layer(50 + bits, 300, 1024, 384, bits, 64, bias=True, outliers=True)
+    d = DeviceLayer(L)
+    check_close(y_to_f64(d.run(lb.PATH_QMM)), _oracle_y(L), f"qmm b={bits}")
+
+
+def test_auto_path_picks_qmm_for_batches():
+    assert lb.select_path(128, 4096, 4096, 4, 128) == lb.PATH_QMM
+    assert lb.select_path(1, 4096, 4096, 4, 128) == lb.PATH_QMV
 
 
 def test_no_wait_timed_out():
