@@ -12,8 +12,10 @@ and zeros, more than the 129 MB L2, so every launch reads its weights cold.
              CUDA graph of 28 C-ABI calls.
   e2e        the same metric with every input copied from pinned host memory
              and y copied back, through the public Python binding, per step.
-  roofline   the qmv kernel alone: per-layer launch time with CUDA events,
-             L2 flushed before each launch, summed over the 28 layers.
+  roofline   the qmv kernel alone: per-layer time (CUDA graphs of flush + call
+             minus flush alone), summed over the 28 layers.
+  qmm_m128   the batched form: the same shapes at M = 128, b = 4, g = 128 on the
+             tensor-core kernel, TFLOP/s against the measured bf16 peak.
   cpu_baseline  the fp64 CPU oracle on a bounded sample of output rows.
 
 ``--impl reference`` times the CPU oracle instead (the method's plain
@@ -254,15 +256,71 @@ def kernel_source_hash():
 
 
 def profiled_traffic():
-    """Per-launch DRAM bytes of the qmv kernel from the committed ncu summary, if that
-    summary was taken on the current kernel source."""
-    p = ROOT / "profiles" / "qmv_llama8b_decode_traffic.json"
+    """Per-launch DRAM bytes (read + write) of the qmv kernel from the committed ncu
+    summary, if that summary was taken on the current kernel source; else None."""
+    p = ROOT / "profiles" / "qmv_stream_llama8b_decode.md"
     if not p.exists():
         return None
-    d = json.loads(p.read_text())
-    if d.get("kernel_source_sha256_16") != kernel_source_hash():
+    fields = {}
+    for line in p.read_text().splitlines():
+        if line.startswith("- ") and ": " in line:
+            k, v = line[2:].split(": ", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
-    return d.get("dram_bytes_per_launch")
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measure_qmm(torch, lb, dev, stream, M=128, bits=4, group=128, reps=10):
+    """The batched form: the same four Llama-3.1-8B shapes at M = 128, b = 4, g = 128, with
+    bias and 1% outlier columns in x, on the tensor-core kernel.  Each layer is timed as a
+    CUDA graph of `reps` calls; TFLOP/s = 2*M*N*K / time."""
+    out = []
+    for name, (K, N) in synth.LLAMA_8B.items():
+        L = synth.make_layer(0, M, K, N, bits, group, bias=True, outliers=True)
+        w = lb.pack_weights(torch.from_numpy(L.codes).to(dev), bits)
+        x = torch.from_numpy(L.x.view(np.int16)).view(torch.bfloat16).to(dev)
+        s = torch.from_numpy(L.scales.view(np.int16)).view(torch.float16).to(dev)
+        z = torch.from_numpy(L.zeros.view(np.int16)).view(torch.float16).to(dev)
+        b = torch.from_numpy(L.bias.view(np.int16)).view(torch.float16).to(dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def call():
+            lb.linear_ptr(x.data_ptr(), w.data_ptr(), s.data_ptr(), z.data_ptr(), b.data_ptr(),
+                          y.data_ptr(), M, K, N, bits, group, stream.cuda_stream, lb.PATH_QMM)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            call()
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(reps):
+                    call()
+        stream.synchronize()
+        best = float("inf")
+        for _ in range(5):
+            a = torch.cuda.Event(enable_timing=True)
+            c = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                g.replay()
+                c.record(stream)
+            stream.synchronize()
+            best = min(best, a.elapsed_time(c) * 1e3 / reps)
+        out.append({"layer": name, "K": K, "N": N, "us": round(best, 2),
+                    "TFLOPs": round(2 * M * N * K / best / 1e6, 1)})
+        del w, x, s, z, b, y, g
+    total_flop = sum(2 * M * o["N"] * o["K"] for o in out)
+    total_us = sum(o["us"] for o in out)
+    tflops = total_flop / total_us / 1e6
+    _, tc_peak, kind = measured_peaks()
+    return {"M": M, "bits": bits, "group": group, "TFLOPs": round(tflops, 1),
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": tc_peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / tc_peak, 4),
+                         "peak_kind": f"{kind} bf16_tflops (burst)"},
+            "layers": out, "timing": "CUDA graph of 10 calls per layer; weights 4-59 MB, L2-warm"}
 
 
 def run_ours(args):
@@ -346,25 +404,42 @@ def run_ours(args):
     value = world * step_bytes * args.steps / (ms_total / 1e3) / 1e9
 
     # --- per-layer kernel time, cold L2 (roofline of the qmv kernel) -------------
+    # CUDA-event timestamps are coarse on this platform (about 2 us), so each layer is
+    # timed as a difference of two CUDA graphs: n x (L2 flush + call) minus n x flush.
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(int(2 * l2), dtype=torch.uint8, device=dev)
-    per_layer = []
-    reps = 20
-    with torch.cuda.stream(stream):
-        for t in layers:
-            times = []
-            for _ in range(reps):
-                flush.fill_(1)
-                a = torch.cuda.Event(enable_timing=True)
-                c = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                call(t, stream.cuda_stream)
-                c.record(stream)
-                times.append((a, c))
+
+    def graph_us(fn, reps=5):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()
             stream.synchronize()
-            us = statistics.median(a.elapsed_time(c) * 1e3 for a, c in times)
-            per_layer.append({"layer": t["name"], "bits": t["b"], "K": t["K"], "N": t["N"],
-                              "us": round(us, 3), "GBps": round(t["bytes"] / us / 1e3, 1)})
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+        stream.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            c = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                g.replay()
+                c.record(stream)
+            stream.synchronize()
+            best = min(best, a.elapsed_time(c) * 1e3)
+        return best
+
+    nrep = 10
+    flush_us = graph_us(lambda: [flush.fill_(i) for i in range(nrep)])
+    per_layer = []
+    for t in layers:
+        def with_call(t=t):
+            for i in range(nrep):
+                flush.fill_(i)
+                call(t, stream.cuda_stream)
+        us = max(graph_us(with_call) - flush_us, 1e-3) / nrep
+        per_layer.append({"layer": t["name"], "bits": t["b"], "K": t["K"], "N": t["N"],
+                          "us": round(us, 3), "GBps": round(t["bytes"] / us / 1e3, 1)})
     del flush
     kern_us = sum(p["us"] for p in per_layer)
     achieved = step_bytes / kern_us / 1e3
@@ -395,6 +470,8 @@ def run_ours(args):
     e2e_ms = dist.max(e0.elapsed_time(e1)) / e2e_steps
     e2e_value = world * step_bytes / (e2e_ms / 1e3) / 1e9
 
+    qmm = None if args.no_qmm else measure_qmm(torch, lb, dev, stream)
+
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -403,7 +480,7 @@ def run_ours(args):
                                    "step_bytes": step_bytes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": profiled_traffic(),
-                     "kernel": "qmv (all 28 layers; per-launch CUDA-event time, L2 flushed)",
+                     "kernel": "qmv_stream (all 28 layers; per-launch time from CUDA graphs, L2 flushed)",
                      "peak_kind": f"{peak_kind} hbm_gbs (burst copy)"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -411,6 +488,8 @@ def run_ours(args):
         "clocks": clk,
         "layers": per_layer,
     }
+    if qmm is not None:
+        line["qmm_m128"] = qmm
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample, rows = calibrate_oracle(args.cpu_seconds)
@@ -424,6 +503,33 @@ def run_ours(args):
     return 0
 
 
+def run_profile_layer(spec: str, calls: int):
+    """Call one layer `calls` times through lowbit_linear, nothing timed: a small, fixed
+    workload for ncu captures.  spec = name:bits:M[:group], name one of qkv/o/gate_up/down."""
+    import torch
+    import bit_groupwise_weight_gb300 as lb
+    from bit_groupwise_weight_gb300 import build as lbuild
+    lbuild.build()
+    parts = spec.split(":")
+    name, bits, M = parts[0], int(parts[1]), int(parts[2])
+    group = int(parts[3]) if len(parts) > 3 else (64 if M <= 2 else 128)
+    K, N = synth.LLAMA_8B[name]
+    L = synth.make_layer(0, M, K, N, bits, group, bias=M > 2, outliers=M > 2)
+    dev = torch.device("cuda", 0)
+    w = lb.pack_weights(torch.from_numpy(L.codes).to(dev), bits)
+    x = torch.from_numpy(L.x.view(np.int16)).view(torch.bfloat16).to(dev)
+    s = torch.from_numpy(L.scales.view(np.int16)).view(torch.float16).to(dev)
+    z = torch.from_numpy(L.zeros.view(np.int16)).view(torch.float16).to(dev)
+    b = None if L.bias is None else torch.from_numpy(L.bias.view(np.int16)).view(torch.float16).to(dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    for _ in range(calls):
+        lb.linear(x, w, s, z, b, bits, group, out=y)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_layer": spec, "calls": calls, "path": lb.select_path(M, K, N, bits, group),
+                      "wait_timeouts": lb.wait_timeouts()}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -432,9 +538,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-qmm", action="store_true", help="skip the secondary M=128 qmm measurement")
+    ap.add_argument("--profile-layer", default=None,
+                    help="name:bits:M[:group] -- only call that layer (for ncu captures)")
+    ap.add_argument("--profile-calls", type=int, default=2)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile_layer:
+        return run_profile_layer(args.profile_layer, args.profile_calls)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -26,9 +26,12 @@
 // 128) codes) accumulates into one of up to four TMEM buffers of TN columns.
 //
 // Warp roles (512 threads):
-//   warp 0       TMA producer: per stage one 2D tensor copy of the 128 x 16b
-//                packed-code tile and two 2D copies (64-wide, 128-byte swizzle)
-//                of the x tile, completing on the stage's mbarrier;
+//   warp 0       TMA producers: lane 0 streams the 128 x 16b packed-code
+//                tiles (one 2D tensor copy per stage) into a deep ring that
+//                the unpackers free; lane 1 streams the x tiles (two 2D copies,
+//                64-wide, 128-byte swizzle) into a ring that MMA completion
+//                frees -- separate rings, so the weights' HBM latency does not
+//                wait on the tensor cores;
 //   warp 1       allocates tensor memory; one lane issues the MMAs
 //                (tcgen05.mma kind::f16, bf16 x bf16 -> fp32) and commits them
 //                to mbarriers that free buffers or hand a segment on;
@@ -53,7 +56,8 @@ namespace {
 constexpr int kBM = 128;             // rows of an A tile (MMA M)
 constexpr int kRowsOut = kBM - 4;    // output rows per tile; rows 31, 63, 95, 127 hold ones
 constexpr int kBK = 128;             // codes per K stage
-constexpr int kInStages = 3;         // packed codes + x ring
+constexpr int kMaxPStages = 8;       // packed-code ring (freed by the unpackers)
+constexpr int kXStages = 3;          // x ring (freed when the MMAs that read it complete)
 constexpr int kAStages = 2;          // code-tile ring
 constexpr int kUnpackWarps = 6;
 constexpr int kAccWarps = 8;
@@ -72,9 +76,9 @@ struct QmmParams {
     const uint16_t *bias;
     uint16_t *y;
     int M, N, K, G, log2g, TN, tmem_cols, nbuf, ktiles, lseg_log2, nseg;
+    int pstages;            // depth of the packed-code ring
     uint32_t x_stage;       // TN * kBK * 2 bytes (two swizzle atoms of TN rows)
-    uint32_t in_stage;      // x_stage + packed tile, rounded to 1024
-    uint32_t a_off, in_off, xs_off;   // offsets from the 1024-aligned base
+    uint32_t a_off, x_off, p_off, xs_off;   // offsets from the 1024-aligned base
     uint32_t idesc;         // tcgen05 instruction descriptor
 };
 
@@ -163,15 +167,20 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
     constexpr uint32_t kPackedStage = kBM * (kBK * BITS / 8);
 
     // Barriers (8 bytes each), then the TMEM address.
-    const uint32_t in_full = base, in_empty = in_full + 8 * kInStages;
-    const uint32_t a_full = in_empty + 8 * kInStages, a_empty = a_full + 8 * kAStages;
+    const uint32_t p_full = base, p_empty = p_full + 8 * kMaxPStages;
+    const uint32_t x_full = p_empty + 8 * kMaxPStages, x_empty = x_full + 8 * kXStages;
+    const uint32_t a_full = x_empty + 8 * kXStages, a_empty = a_full + 8 * kAStages;
     const uint32_t t_full = a_empty + 8 * kAStages, t_empty = t_full + 8 * kMaxTmemBufs;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + (t_empty + 8 * kMaxTmemBufs - base));
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kInStages; ++i) {
-            ptx::mbar_init(in_full + 8 * i, 1);
-            ptx::mbar_init(in_empty + 8 * i, kUnpackWarps + 1);
+        for (int i = 0; i < p.pstages; ++i) {
+            ptx::mbar_init(p_full + 8 * i, 1);
+            ptx::mbar_init(p_empty + 8 * i, kUnpackWarps);
+        }
+        for (int i = 0; i < kXStages; ++i) {
+            ptx::mbar_init(x_full + 8 * i, 1);
+            ptx::mbar_init(x_empty + 8 * i, 1);
         }
         for (int i = 0; i < kAStages; ++i) {
             ptx::mbar_init(a_full + 8 * i, kUnpackWarps);
@@ -203,42 +212,48 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
     const uint32_t tmem = *tmem_slot;
 
     const uint32_t a_base = base + p.a_off;
-    const uint32_t in_base = base + p.in_off;
+    const uint32_t x_base = base + p.x_off;
+    const uint32_t p_base = base + p.p_off;
     const int lseg = 1 << p.lseg_log2;           // codes per segment (min(g, 128))
     const int sps = kBK >> p.lseg_log2;          // segments per stage
 
     if (warp == 0) {
-        // ---------------- TMA producer.
-        if (lane == 0) {
+        // ---------------- TMA producers (lane 0: packed codes, lane 1: x).
+        if (lane < 2) {
+            const int depth = lane == 0 ? p.pstages : kXStages;
+            const uint32_t full = lane == 0 ? p_full : x_full;
+            const uint32_t empty = lane == 0 ? p_empty : x_empty;
             const uint64_t pol = ptx::policy_evict_first();
             int issued = 0;
             for (int kt = 0; kt < p.ktiles; ++kt, ++issued) {
-                const int st = kt % kInStages;
-                if (kt >= kInStages &&
-                    !ptx::mbar_wait(in_empty + 8 * st, ((kt / kInStages) - 1) & 1, &g_qmm_timeouts))
+                const int st = kt % depth;
+                if (kt >= depth && !ptx::mbar_wait(empty + 8 * st, ((kt / depth) - 1) & 1, &g_qmm_timeouts))
                     break;
-                const uint32_t bar = in_full + 8 * st;
-                const uint32_t xs = in_base + st * p.in_stage;
-                ptx::mbar_arrive_expect_tx(bar, p.x_stage + kPackedStage);
-                ptx::tma_load_2d(xs, &xmap, kt * kBK, m0, bar);
-                ptx::tma_load_2d(xs + p.x_stage / 2, &xmap, kt * kBK + 64, m0, bar);
-                ptx::tma_load_2d_hint(xs + p.x_stage, &wmap, kt * (kBK * BITS / 8), n0, bar, pol);
+                const uint32_t bar = full + 8 * st;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(bar, kPackedStage);
+                    ptx::tma_load_2d_hint(p_base + st * kPackedStage, &wmap, kt * (kBK * BITS / 8), n0, bar, pol);
+                } else {
+                    const uint32_t xs = x_base + st * p.x_stage;
+                    ptx::mbar_arrive_expect_tx(bar, p.x_stage);
+                    ptx::tma_load_2d(xs, &xmap, kt * kBK, m0, bar);
+                    ptx::tma_load_2d(xs + p.x_stage / 2, &xmap, kt * kBK + 64, m0, bar);
+                }
             }
-            for (int i = max(0, issued - kInStages); i < issued; ++i)
-                if (!ptx::mbar_wait(in_full + 8 * (i % kInStages), (i / kInStages) & 1, &g_qmm_timeouts))
-                    break;
+            for (int i = max(0, issued - depth); i < issued; ++i)
+                if (!ptx::mbar_wait(full + 8 * (i % depth), (i / depth) & 1, &g_qmm_timeouts)) break;
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer.
         if (lane == 0) {
             bool ok = true;
             for (int kt = 0; kt < p.ktiles && ok; ++kt) {
-                const int st = kt % kInStages, as = kt % kAStages;
-                ok = ptx::mbar_wait(in_full + 8 * st, (kt / kInStages) & 1, &g_qmm_timeouts) &&
+                const int st = kt % kXStages, as = kt % kAStages;
+                ok = ptx::mbar_wait(x_full + 8 * st, (kt / kXStages) & 1, &g_qmm_timeouts) &&
                      ptx::mbar_wait(a_full + 8 * as, (kt / kAStages) & 1, &g_qmm_timeouts);
                 if (!ok) break;
                 const uint32_t a_st = a_base + as * kAStageBytes;
-                const uint32_t x_st = in_base + st * p.in_stage;
+                const uint32_t x_st = x_base + st * p.x_stage;
                 for (int sg = 0; sg < sps && ok; ++sg) {
                     const int seg = kt * sps + sg;
                     const int b = seg % p.nbuf;
@@ -255,26 +270,31 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
                     }
                     ptx::mma_commit(t_full + 8 * b);
                 }
-                ptx::mma_commit(in_empty + 8 * st);
+                ptx::mma_commit(x_empty + 8 * st);
                 ptx::mma_commit(a_empty + 8 * as);
             }
         }
     } else if (warp < kFirstAccWarp) {
         // ---------------- code unpackers (warps 2..7): 124 rows x 4 blocks per stage.
-        const int ut = (warp - kFirstUnpackWarp) * 32 + lane;    // 0..191
+        // A warp covers 8 rows x 4 blocks; lane -> (block, row) is chosen so that
+        // every 8-lane phase of a 16-byte store hits 8 different bank groups of the
+        // swizzled tile: lanes 0-15 take blocks 0/1 of rows 0..7, lanes 16-31 blocks 2/3.
+        const int ublk = (lane & 1) | ((lane >> 4) << 1);
+        const int urow = (lane >> 1) & 7;
+        const int uw = warp - kFirstUnpackWarp;
         bool ok = true;
         for (int kt = 0; kt < p.ktiles && ok; ++kt) {
-            const int st = kt % kInStages, as = kt % kAStages;
-            ok = ptx::mbar_wait(in_full + 8 * st, (kt / kInStages) & 1, &g_qmm_timeouts);
+            const int st = kt % p.pstages, as = kt % kAStages;
+            ok = ptx::mbar_wait(p_full + 8 * st, (kt / p.pstages) & 1, &g_qmm_timeouts);
             if (ok && kt >= kAStages)
                 ok = ptx::mbar_wait(a_empty + 8 * as, ((kt / kAStages) - 1) & 1, &g_qmm_timeouts);
             if (!ok) break;
-            const uint8_t *pk = smem + p.in_off + st * p.in_stage + p.x_stage;
+            const uint8_t *pk = smem + p.p_off + st * kPackedStage;
             uint8_t *a_st = smem + p.a_off + as * kAStageBytes;
 #pragma unroll
             for (int i = 0; i < 3; ++i) {
-                const int task = ut + kUnpackWarps * 32 * i;
-                const int pr = task >> 2, blk = task & 3;     // packed row within the tile
+                const int pr = (uw + kUnpackWarps * i) * 8 + urow;   // packed row within the tile
+                const int blk = ublk;
                 if (pr < kRowsOut) {
                     const int r = pr + pr / 31;               // A row: skip the ones rows
                     uint32_t w[BITS];
@@ -292,7 +312,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
             ptx::fence_proxy_async_smem();      // generic-proxy stores -> tensor-core reads
             __syncwarp();
             if (lane == 0) {
-                ptx::mbar_arrive(in_empty + 8 * st);
+                ptx::mbar_arrive(p_empty + 8 * st);
                 ptx::mbar_arrive(a_full + 8 * as);
             }
         }
@@ -313,11 +333,19 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
             for (int j = 0; j < 8; ++j) acc[c][j] = make_float2(0.f, 0.f);
         bool ok = true;
         const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+        // Scale and zero of segment seg+2 are fetched while segment seg is processed.
+        const uint16_t *srow = p.s + (int64_t)nrow * p.G, *zrow = p.z + (int64_t)nrow * p.G;
+        auto seg_group = [&](int sg) { return min((sg << p.lseg_log2) >> p.log2g, p.G - 1); };
+        uint16_t s0 = __ldg(srow + seg_group(0)), s1 = __ldg(srow + seg_group(1));
+        uint16_t z0 = __ldg(zrow + seg_group(0)), z1 = __ldg(zrow + seg_group(1));
         for (int seg = 0; seg < p.nseg; ++seg) {
             const int b = seg % p.nbuf;
-            const int gi = (seg << p.lseg_log2) >> p.log2g;
-            const float sv = half_bits_to_float(__ldg(p.s + (int64_t)nrow * p.G + gi));
-            const float zv = half_bits_to_float(__ldg(p.z + (int64_t)nrow * p.G + gi));
+            const float sv = half_bits_to_float(s0);
+            const float zv = half_bits_to_float(z0);
+            s0 = s1;
+            z0 = z1;
+            s1 = __ldg(srow + seg_group(seg + 2));
+            z1 = __ldg(zrow + seg_group(seg + 2));
             const float2 s2 = make_float2(sv, sv);
             const float zc = fmaf(-128.f, sv, zv);      // zero minus the codes' +128 offset
             const float2 z2 = make_float2(zc, zc);
@@ -430,11 +458,13 @@ cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, 
     q.nseg = K >> q.lseg_log2;
     q.x_stage = (uint32_t)q.TN * kBK * 2u;
     const uint32_t packed = kBM * (kBK * BITS / 8);
-    q.in_stage = (q.x_stage + packed + 1023u) & ~1023u;
-    q.xs_off = 256;                                   // 8 warps x 32 fp32 group sums
+    q.xs_off = 512;                                   // 8 warps x 32 fp32 group sums
     q.a_off = 2048;
-    q.in_off = q.a_off + kAStages * kAStageBytes;
-    const uint32_t smem = 1024u + q.in_off + kInStages * q.in_stage;   // + alignment slack
+    q.x_off = q.a_off + kAStages * kAStageBytes;
+    q.p_off = q.x_off + kXStages * q.x_stage;
+    const uint32_t budget = 226u * 1024u - 1024u;     // minus alignment slack
+    q.pstages = (int)std::min<uint32_t>(kMaxPStages, (budget - q.p_off) / packed);
+    const uint32_t smem = 1024u + q.p_off + q.pstages * packed;
     q.idesc = (1u << 4)                        // accumulate in fp32
             | (1u << 7) | (1u << 10)           // A and B are bf16
             | ((uint32_t)(q.TN >> 3) << 17)    // N
