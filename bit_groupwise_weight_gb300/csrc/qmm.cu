@@ -21,23 +21,26 @@
 // tile covers 124 output rows.
 //
 // Tiling ("swap AB"): the MMA's 128-row A operand is a tile of weight rows
-// (output features n); its B operand is a tile of TN rows of x (TN <= 128,
-// batch rows m).  K advances 128 codes per stage; each group segment (min(g,
-// 128) codes) accumulates into one of up to four TMEM buffers of TN columns.
+// (output features n), held in tensor memory; its B operand is a tile of TN
+// rows of x (TN <= 128, batch rows m) in shared memory.  K advances 128 codes
+// per stage; each group segment (min(g, 128) codes) accumulates into one of
+// several TMEM buffers of TN columns.  Keeping A in tensor memory means the
+// unpacked codes never travel through shared memory (neither as stores nor as
+// MMA operand reads), which leaves shared-memory bandwidth to the x tiles.
 //
-// Warp roles (512 threads):
+// Warp roles (448 threads):
 //   warp 0       TMA producers: lane 0 streams the 128 x 16b packed-code
 //                tiles (one 2D tensor copy per stage) into a deep ring that
 //                the unpackers free; lane 1 streams the x tiles (two 2D copies,
 //                64-wide, 128-byte swizzle) into a ring that MMA completion
-//                frees -- separate rings, so the weights' HBM latency does not
-//                wait on the tensor cores;
+//                frees;
 //   warp 1       allocates tensor memory; one lane issues the MMAs
-//                (tcgen05.mma kind::f16, bf16 x bf16 -> fp32) and commits them
-//                to mbarriers that free buffers or hand a segment on;
-//   warps 2..7   unpack codes into bf16 pairs in the 128-byte-swizzled
-//                K-major layout the MMA reads;
-//   warps 8..15  accumulate: per segment read P_g and X_g from tensor memory,
+//                (tcgen05.mma kind::f16, A from tensor memory, bf16 x bf16 ->
+//                fp32) and commits them to mbarriers that free buffers or hand
+//                a segment on;
+//   warps 2..5   unpack: one thread per tile row (its TMEM lane) turns the
+//                row's codes into bf16 pairs and writes them with tcgen05.st;
+//   warps 6..13  accumulate: per segment read P_g and X_g from tensor memory,
 //                apply scale and zero in fp32, and at the end add the bias and
 //                store y (two warps per tensor-memory lane quarter).
 // All waits are bounded (about one second) and count a timeout instead of
@@ -56,16 +59,16 @@ namespace {
 constexpr int kBM = 128;             // rows of an A tile (MMA M)
 constexpr int kRowsOut = kBM - 4;    // output rows per tile; rows 31, 63, 95, 127 hold ones
 constexpr int kBK = 128;             // codes per K stage
-constexpr int kMaxPStages = 8;       // packed-code ring (freed by the unpackers)
-constexpr int kXStages = 3;          // x ring (freed when the MMAs that read it complete)
-constexpr int kAStages = 2;          // code-tile ring
-constexpr int kUnpackWarps = 6;
+constexpr int kMaxPStages = 12;      // packed-code ring (freed by the unpackers)
+constexpr int kXStages = 4;          // x ring (freed when the MMAs that read it complete)
+constexpr int kAStages = 2;          // code tiles in tensor memory
+constexpr int kACols = kBK / 2;      // TMEM columns of one code tile (two bf16 per column)
+constexpr int kUnpackWarps = 4;      // one per TMEM lane quarter
 constexpr int kAccWarps = 8;
 constexpr int kFirstUnpackWarp = 2;
-constexpr int kFirstAccWarp = kFirstUnpackWarp + kUnpackWarps;    // 8
-constexpr int kThreads = (kFirstAccWarp + kAccWarps) * 32;        // 512
+constexpr int kFirstAccWarp = kFirstUnpackWarp + kUnpackWarps;    // 6
+constexpr int kThreads = (kFirstAccWarp + kAccWarps) * 32;        // 448
 constexpr int kMaxTmemBufs = 4;
-constexpr uint32_t kAStageBytes = kBM * kBK * 2;                  // two 64-column swizzle atoms
 constexpr uint32_t kBf16Magic = 0x43004300u;                      // bf16 pair (128, 128)
 
 __device__ unsigned int g_qmm_timeouts;
@@ -75,10 +78,10 @@ struct QmmParams {
     const uint16_t *z;
     const uint16_t *bias;
     uint16_t *y;
-    int M, N, K, G, log2g, TN, tmem_cols, nbuf, ktiles, lseg_log2, nseg;
+    int M, N, K, G, log2g, TN, tmem_cols, nbuf, a_col, ktiles, lseg_log2, nseg;
     int pstages;            // depth of the packed-code ring
     uint32_t x_stage;       // TN * kBK * 2 bytes (two swizzle atoms of TN rows)
-    uint32_t a_off, x_off, p_off, xs_off;   // offsets from the 1024-aligned base
+    uint32_t x_off, p_off, xs_off;   // offsets from the 1024-aligned base
     uint32_t idesc;         // tcgen05 instruction descriptor
 };
 
@@ -145,13 +148,6 @@ __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t (&w)[BITS])
     }
 }
 
-// Byte address of the 16-byte chunk `chunk` (0..15 along K) of row r in a
-// 128 x 128 bf16 tile stored as two 128-byte-swizzled K-major atoms.
-__device__ __forceinline__ uint32_t a_chunk_offset(int r, int chunk) {
-    return (uint32_t)((chunk >> 3) * (kBM * 128) + (r >> 3) * 1024 + (r & 7) * 128 +
-                      (((chunk & 7) ^ (r & 7)) << 4));
-}
-
 template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
@@ -196,22 +192,12 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
         ptx::tmem_relinquish();
     }
-    // Rows 31, 63, 95, 127 of both A stages: bf16 ones (written once, never overwritten).
-    if (warp >= kFirstUnpackWarp && warp < kFirstAccWarp) {
-        const int t = (warp - kFirstUnpackWarp) * 32 + lane;    // (stage, quarter, chunk)
-        if (t < kAStages * 4 * 16) {
-            uint8_t *a_st = smem + p.a_off + (t >> 6) * kAStageBytes;
-            *reinterpret_cast<uint4 *>(a_st + a_chunk_offset(((t >> 4) & 3) * 32 + 31, t & 15)) =
-                make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        }
-        ptx::fence_proxy_async_smem();
-    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const uint32_t a_base = base + p.a_off;
+    const uint32_t a_tmem = tmem + (uint32_t)p.a_col;    // code tiles: kAStages x kACols columns
     const uint32_t x_base = base + p.x_off;
     const uint32_t p_base = base + p.p_off;
     const int lseg = 1 << p.lseg_log2;           // codes per segment (min(g, 128))
@@ -252,7 +238,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
                 ok = ptx::mbar_wait(x_full + 8 * st, (kt / kXStages) & 1, &g_qmm_timeouts) &&
                      ptx::mbar_wait(a_full + 8 * as, (kt / kAStages) & 1, &g_qmm_timeouts);
                 if (!ok) break;
-                const uint32_t a_st = a_base + as * kAStageBytes;
+                const uint32_t a_st = a_tmem + (uint32_t)(as * kACols);
                 const uint32_t x_st = x_base + st * p.x_stage;
                 for (int sg = 0; sg < sps && ok; ++sg) {
                     const int seg = kt * sps + sg;
@@ -264,9 +250,9 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
                     const int kk0 = sg * (lseg / 16);
                     for (int kk = kk0; kk < kk0 + lseg / 16; ++kk) {
                         const uint32_t atom = kk >> 2, koff = (kk & 3) * 32;
-                        const uint64_t ad = ptx::sw128_desc(a_st + atom * (kBM * 128) + koff);
                         const uint64_t bd = ptx::sw128_desc(x_st + atom * (p.x_stage / 2) + koff);
-                        ptx::mma_f16(tmem + (uint32_t)(b * p.TN), ad, bd, p.idesc, kk != kk0);
+                        ptx::mma_f16_tmem_a(tmem + (uint32_t)(b * p.TN), a_st + (uint32_t)(kk * 8), bd, p.idesc,
+                                            kk != kk0);
                     }
                     ptx::mma_commit(t_full + 8 * b);
                 }
@@ -275,13 +261,10 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
             }
         }
     } else if (warp < kFirstAccWarp) {
-        // ---------------- code unpackers (warps 2..7): 124 rows x 4 blocks per stage.
-        // A warp covers 8 rows x 4 blocks; lane -> (block, row) is chosen so that
-        // every 8-lane phase of a 16-byte store hits 8 different bank groups of the
-        // swizzled tile: lanes 0-15 take blocks 0/1 of rows 0..7, lanes 16-31 blocks 2/3.
-        const int ublk = (lane & 1) | ((lane >> 4) << 1);
-        const int urow = (lane >> 1) & 7;
-        const int uw = warp - kFirstUnpackWarp;
+        // ---------------- code unpackers (warps 2..5): thread = one tile row = its TMEM lane.
+        const int q = warp & 3;
+        const int pr = q * 31 + lane;                    // packed row in the tile (lane 31: ones row)
+        const uint32_t trow = ((uint32_t)(q * 32) << 16);
         bool ok = true;
         for (int kt = 0; kt < p.ktiles && ok; ++kt) {
             const int st = kt % p.pstages, as = kt % kAStages;
@@ -289,27 +272,26 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
             if (ok && kt >= kAStages)
                 ok = ptx::mbar_wait(a_empty + 8 * as, ((kt / kAStages) - 1) & 1, &g_qmm_timeouts);
             if (!ok) break;
-            const uint8_t *pk = smem + p.p_off + st * kPackedStage;
-            uint8_t *a_st = smem + p.a_off + as * kAStageBytes;
+            ptx::tc_fence_after();
+            const uint8_t *pk = smem + p.p_off + st * kPackedStage + pr * (kBK * BITS / 8);
+            const uint32_t adst = a_tmem + trow + (uint32_t)(as * kACols);
 #pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                const int pr = (uw + kUnpackWarps * i) * 8 + urow;   // packed row within the tile
-                const int blk = ublk;
-                if (pr < kRowsOut) {
-                    const int r = pr + pr / 31;               // A row: skip the ones rows
+            for (int blk = 0; blk < 4; ++blk) {
+                uint32_t h[16];
+                if (lane < 31) {
                     uint32_t w[BITS];
-                    lds_words<BITS>(pk + (pr * (kBK / 32) + blk) * (4 * BITS), w);
-                    uint32_t h[16];
+                    lds_words<BITS>(pk + blk * (4 * BITS), w);
                     [&]<int... J>(std::integer_sequence<int, J...>) {
                         ((h[J] = code_pair<BITS, J>(w)), ...);
                     }(std::make_integer_sequence<int, 16>{});
+                } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4 *>(a_st + a_chunk_offset(r, blk * 4 + c)) =
-                            make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                    for (int j = 0; j < 16; ++j) h[j] = 0x3F803F80u;   // bf16 (1, 1)
                 }
+                ptx::tmem_st16(adst + (uint32_t)(blk * 16), h);
             }
-            ptx::fence_proxy_async_smem();      // generic-proxy stores -> tensor-core reads
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 ptx::mbar_arrive(p_empty + 8 * st);
@@ -450,8 +432,9 @@ cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, 
     q.s = s; q.z = z; q.bias = bias; q.y = y;
     q.M = M; q.N = N; q.K = K; q.G = K / group; q.log2g = __builtin_ctz((unsigned)group);
     q.TN = M >= 128 ? 128 : ((M + 15) / 16) * 16;
-    q.nbuf = std::min(kMaxTmemBufs, 512 / q.TN);
-    const int cols = q.nbuf * q.TN;
+    q.nbuf = std::min(kMaxTmemBufs, (512 - kAStages * kACols) / q.TN);
+    q.a_col = q.nbuf * q.TN;
+    const int cols = q.a_col + kAStages * kACols;
     q.tmem_cols = cols <= 32 ? 32 : (cols <= 64 ? 64 : (cols <= 128 ? 128 : (cols <= 256 ? 256 : 512)));
     q.ktiles = K / kBK;
     q.lseg_log2 = std::min(q.log2g, 7);
@@ -459,8 +442,7 @@ cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, 
     q.x_stage = (uint32_t)q.TN * kBK * 2u;
     const uint32_t packed = kBM * (kBK * BITS / 8);
     q.xs_off = 512;                                   // 8 warps x 32 fp32 group sums
-    q.a_off = 2048;
-    q.x_off = q.a_off + kAStages * kAStageBytes;
+    q.x_off = 2048;
     q.p_off = q.x_off + kXStages * q.x_stage;
     const uint32_t budget = 226u * 1024u - 1024u;     // minus alignment slack
     q.pstages = (int)std::min<uint32_t>(kMaxPStages, (budget - q.p_off) / packed);
