@@ -90,6 +90,26 @@ __device__ __forceinline__ void load_block(const uint8_t *p, uint32_t (&w)[BITS]
     }
 }
 
+// Launch `kernel` with programmatic stream serialisation: the kernel may begin
+// while the previous kernel in the stream finishes, and must call
+// griddepcontrol.wait before touching global memory (every kernel launched
+// this way here does so first thing).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 }  // namespace lowbit
 
 // Launchers implemented in the .cu files (host side, no argument checks: the

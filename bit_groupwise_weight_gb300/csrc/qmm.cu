@@ -157,6 +157,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
     const uint32_t base = (raw + 1023u) & ~1023u;            // swizzle atoms need 1024-byte alignment
     uint8_t *smem = smem_raw + (base - raw);
 
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();            // inputs may come from the previous kernel in the stream
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kRowsOut;
     const int m0 = blockIdx.y * p.TN;
@@ -480,8 +482,8 @@ cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, 
         g_smem_attr_set[BITS].store(1, std::memory_order_relaxed);
     }
     const dim3 grid((N + kRowsOut - 1) / kRowsOut, (M + q.TN - 1) / q.TN);
-    qmm_kernel<BITS><<<grid, kThreads, smem, stream>>>(xmap, wmap, q);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(qmm_kernel<BITS>, grid, dim3(kThreads), smem, stream, xmap, wmap, q);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -375,6 +375,8 @@ qmv_stream_kernel(const StreamParams p) {
     const int S = p.stages;
 
     // This CTA's passes [pass0, pass0 + npass).
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();            // inputs may come from the previous kernel in the stream
     const int c = blockIdx.x;
     const int ch0 = c * p.chunks_base + min(c, p.chunks_extra);
     const int nch = p.chunks_base + (c < p.chunks_extra ? 1 : 0);
@@ -631,8 +633,9 @@ StreamPlan plan_stream(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
 
 template <int BITS, int M>
 cudaError_t launch_stream(const StreamPlan &pl, cudaStream_t stream) {
-    qmv_stream_kernel<BITS, M><<<pl.grid, pl.threads, pl.smem, stream>>>(pl.prm);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(qmv_stream_kernel<BITS, M>, dim3(pl.grid), dim3(pl.threads), pl.smem,
+                               stream, pl.prm);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int BITS>
