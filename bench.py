@@ -16,6 +16,8 @@ and zeros, more than the 129 MB L2, so every launch reads its weights cold.
              minus flush alone), summed over the 28 layers.
   qmm_m128   the batched form: the same shapes at M = 128, b = 4, g = 128 on the
              tensor-core kernel, TFLOP/s against the measured bf16 peak.
+  quantize   the GPU quantiser on the gate+up weight (bf16, b = 4, g = 64),
+             GB/s against the measured HBM peak.
   cpu_baseline  the fp64 CPU oracle on a bounded sample of output rows.
 
 ``--impl reference`` times the CPU oracle instead (the method's plain
@@ -323,6 +325,45 @@ def measure_qmm(torch, lb, dev, stream, M=128, bits=4, group=128, reps=10):
             "layers": out, "timing": "CUDA graph of 10 calls per layer; weights 4-59 MB, L2-warm"}
 
 
+def measure_quantize(torch, lb, dev, stream, bits=4, group=64, reps=5):
+    """The quantiser on the largest Llama-3.1-8B weight (gate+up, K=4096, N=28672) in bf16:
+    235 MB read per call, more than L2, so back-to-back calls stream from HBM.
+    GB/s = (weights read + packed codes, scales and zeros written) / time."""
+    K, N = synth.LLAMA_8B["gate_up"]
+    w32 = synth.make_weights(0, N, K)
+    w = torch.from_numpy(synth.f32_to_bf16_bits(w32).view(np.int16)).view(torch.bfloat16).to(dev)
+    packed = torch.empty((N, K * bits // 8), dtype=torch.uint8, device=dev)
+    sc = torch.empty((N, K // group), dtype=torch.float16, device=dev)
+    ze = torch.empty((N, K // group), dtype=torch.float16, device=dev)
+    with torch.cuda.stream(stream):
+        lb.quantize_weights(w, bits, group, packed, sc, ze)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                lb.quantize_weights(w, bits, group, packed, sc, ze)
+    stream.synchronize()
+    best = float("inf")
+    for _ in range(5):
+        a = torch.cuda.Event(enable_timing=True)
+        c = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            c.record(stream)
+        stream.synchronize()
+        best = min(best, a.elapsed_time(c) * 1e3 / reps)
+    nbytes = N * K * 2 + N * K * bits // 8 + 4 * N * (K // group)
+    gbs = nbytes / best / 1e3
+    hbm_peak, _, kind = measured_peaks()
+    return {"layer": "gate_up", "K": K, "N": N, "bits": bits, "group": group, "w_dtype": "bf16",
+            "us": round(best, 2), "bytes": nbytes,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                         "peak_kind": f"{kind} hbm_gbs (burst copy)"},
+            "timing": f"CUDA graph of {reps} calls; 235 MB of weights per call (> L2)"}
+
+
 def run_ours(args):
     import torch
     import bit_groupwise_weight_gb300 as lb
@@ -471,6 +512,7 @@ def run_ours(args):
     e2e_value = world * step_bytes / (e2e_ms / 1e3) / 1e9
 
     qmm = None if args.no_qmm else measure_qmm(torch, lb, dev, stream)
+    quant = None if args.no_quantize else measure_quantize(torch, lb, dev, stream)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -490,6 +532,8 @@ def run_ours(args):
     }
     if qmm is not None:
         line["qmm_m128"] = qmm
+    if quant is not None:
+        line["quantize"] = quant
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample, rows = calibrate_oracle(args.cpu_seconds)
@@ -539,6 +583,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-qmm", action="store_true", help="skip the secondary M=128 qmm measurement")
+    ap.add_argument("--no-quantize", action="store_true",
+                    help="skip the secondary quantiser measurement")
     ap.add_argument("--profile-layer", default=None,
                     help="name:bits:M[:group] -- only call that layer (for ncu captures)")
     ap.add_argument("--profile-calls", type=int, default=2)

@@ -7,6 +7,7 @@ CUDA kernels; there is no CPU or PyTorch fallback, and every function raises
 if the compiled library is missing.
 
     packed = pack_weights(codes, bits)            # codes: uint8 [N, K] on cuda
+    packed, scales, zeros = quantize_weights(w, bits=4, group=64)   # w: float [N, K]
     y = linear(x, packed, scales, zeros, bias, bits=4, group=64)
 """
 from __future__ import annotations
@@ -21,6 +22,7 @@ from ._abi import (  # noqa: F401
     linear_ptr,
     pack_weights,
     packed_bytes,
+    quantize_weights,
     select_path,
     status_string,
     unpack_weights,
@@ -29,6 +31,6 @@ from ._abi import (  # noqa: F401
 
 __all__ = [
     "LowbitError", "PATH_AUTO", "PATH_QMM", "PATH_QMV", "abi", "linear", "linear_ptr",
-    "pack_weights", "packed_bytes", "select_path", "status_string", "unpack_weights",
+    "pack_weights", "packed_bytes", "quantize_weights", "select_path", "status_string", "unpack_weights",
     "wait_timeouts",
 ]

@@ -16,6 +16,7 @@ from . import build as _build
 
 LOWBIT_OK, LOWBIT_EINVAL, LOWBIT_EUNSUPPORTED, LOWBIT_ECUDA = 0, 1, 2, 3
 PATH_AUTO, PATH_QMV, PATH_QMM = 0, 1, 2
+DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
 
 _lib = None
 
@@ -36,6 +37,8 @@ def _bind(lib):
     lib.lowbit_pack_weights.restype = ci
     lib.lowbit_unpack_weights.argtypes = [vp, vp, i64, i64, ci, vp]
     lib.lowbit_unpack_weights.restype = ci
+    lib.lowbit_quantize_weights.argtypes = [vp, ci, vp, vp, vp, i64, i64, ci, ci, vp]
+    lib.lowbit_quantize_weights.restype = ci
     lib.lowbit_linear.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, vp]
     lib.lowbit_linear.restype = ci
     lib.lowbit_linear_ex.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, vp]
@@ -127,6 +130,33 @@ def unpack_weights(packed: torch.Tensor, K: int, bits: int, out: torch.Tensor | 
     _check(abi().lowbit_unpack_weights(packed.data_ptr(), out.data_ptr(), N, K, bits,
                                        _stream(packed.device)), "lowbit_unpack_weights")
     return out
+
+
+_W_DTYPES = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16}
+
+
+def quantize_weights(w: torch.Tensor, bits: int, group: int, packed: torch.Tensor | None = None,
+                     scales: torch.Tensor | None = None, zeros: torch.Tensor | None = None):
+    """w float32/bfloat16/float16 [N, K] -> (packed uint8 [N, K*bits/8],
+    scales fp16 [N, K/group], zeros fp16 [N, K/group]), min/max asymmetric."""
+    N, K = w.shape
+    if w.dtype not in _W_DTYPES:
+        raise ValueError(f"w must be float32, bfloat16 or float16, got {w.dtype}")
+    _need(w, "w", w.dtype, (N, K))
+    G = K // group if group else 0
+    if packed is None:
+        packed = torch.empty((N, K * bits // 8), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((N, G), dtype=torch.float16, device=w.device)
+    if zeros is None:
+        zeros = torch.empty((N, G), dtype=torch.float16, device=w.device)
+    _need(packed, "packed", torch.uint8, (N, K * bits // 8))
+    _need(scales, "scales", torch.float16, (N, G))
+    _need(zeros, "zeros", torch.float16, (N, G))
+    _check(abi().lowbit_quantize_weights(w.data_ptr(), _W_DTYPES[w.dtype], packed.data_ptr(),
+                                         scales.data_ptr(), zeros.data_ptr(), N, K, bits, group,
+                                         _stream(w.device)), "lowbit_quantize_weights")
+    return packed, scales, zeros
 
 
 def linear(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,

@@ -101,6 +101,24 @@ lowbit_status lowbit_unpack_weights(const uint8_t *packed, uint8_t *codes, int64
     return from_cuda(lowbit::launch_unpack(packed, codes, N, K, bits, (cudaStream_t)stream));
 }
 
+lowbit_status lowbit_quantize_weights(const void *w, lowbit_dtype dtype, uint8_t *packed,
+                                      uint16_t *scales, uint16_t *zeros, int64_t N, int64_t K,
+                                      int bits, int group, lowbit_stream_t stream) {
+    if (!bits_ok(bits) || !group_ok(group) || N < 0 || K <= 0 || N > kMaxDim || K > kMaxDim ||
+        K % group != 0)
+        return LOWBIT_EINVAL;
+    if (dtype != LOWBIT_DTYPE_F32 && dtype != LOWBIT_DTYPE_BF16 && dtype != LOWBIT_DTYPE_F16)
+        return LOWBIT_EINVAL;
+    if (N == 0) return LOWBIT_OK;
+    if (!w || !packed || !scales || !zeros) return LOWBIT_EINVAL;
+    if (!aligned(w, 16) || !aligned(scales, 2) || !aligned(zeros, 2))
+        return LOWBIT_EINVAL;
+    lowbit_status st = check_device();
+    if (st != LOWBIT_OK) return st;
+    return from_cuda(lowbit::launch_quantize(w, (int)dtype, packed, scales, zeros, N, K, bits,
+                                             group, (cudaStream_t)stream));
+}
+
 lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int group) {
     if (!bits_ok(bits) || !group_ok(group) || M < 0 || N < 0 || K <= 0 || K % group != 0 ||
         M > kMaxDim || N > kMaxDim || K > kMaxDim)

@@ -122,6 +122,9 @@ cudaError_t launch_unpack(const uint8_t *packed, uint8_t *codes, int64_t N, int6
 cudaError_t launch_qmv(const uint16_t *x, const uint8_t *w, const uint16_t *scales,
                        const uint16_t *zeros, const uint16_t *bias, uint16_t *y, int64_t M,
                        int64_t K, int64_t N, int bits, int group, cudaStream_t stream);
+cudaError_t launch_quantize(const void *w, int dtype, uint8_t *packed, uint16_t *scales,
+                            uint16_t *zeros, int64_t N, int64_t K, int bits, int group,
+                            cudaStream_t stream);
 // Bounded waits that gave up, per kernel file (device counters; reading syncs).
 uint32_t qmv_timeouts(bool reset);
 uint32_t qmm_timeouts(bool reset);

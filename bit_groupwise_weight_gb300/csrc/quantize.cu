@@ -1,0 +1,221 @@
+// quantize.cu -- groupwise asymmetric quantisation of a weight matrix, fused
+// with packing.
+//
+// The pages name a `_quantize` function producing the codes and the
+// N x num_groups scales and zeros (ao PR #2167 "metal lowbit kernels:
+// qmv_fast optimization", Summary, bullet 1) without defining it; the
+// min/max reading used throughout this library:
+//   zero  = fp16 rounded toward -inf of min(w over the group)
+//   scale = fp16 rounded toward +inf of (max - zero) / (2^b - 1)
+//   q     = clamp(round-half-even((w - zero) / scale), 0, 2^b - 1)
+//   a constant group (max == min): scale = 2^-14 (smallest fp16 normal), q = 0.
+// The result is defined by fp64 arithmetic on the exact inputs.  The kernel
+// reaches the same bits with fp32 arithmetic wherever fp32 provably decides
+// the same way, and falls back to fp64 where it cannot tell:
+//   - min and max are exact in fp32 (the inputs are fp32, bf16 or fp16);
+//   - the fp64 scale quotient lies between the fp32 quotients rounded down
+//     and up, so when both round up to the same fp16 that fp16 is the scale;
+//   - (w - zero) / scale in fp32 is within 2^-14 of the fp64 quotient (it is
+//     at most 2^7 and carries three roundings of 2^-24 relative), so its
+//     round-half-even agrees with fp64's unless it lies within that distance
+//     of a half-integer; codes closer than 2^-10 to one are recomputed in fp64.
+// The codes are written packed (contiguous, LSB-first, ao PR #2167 Summary
+// bullet 2).
+//
+// Work unit: one warp per chunk of 256 consecutive weights of a row.  Lane l
+// loads weights [8l, 8l+8) with 16-byte loads; a group of g weights spans g/8
+// lanes, whose min/max is a segmented shuffle reduction; the lane's 8 codes
+// are one octet, written as b bytes at byte l*b of the chunk's packed bytes.
+#include "common.cuh"
+
+namespace lowbit {
+namespace {
+
+constexpr int kChunk = 256;          // weights per warp per step
+
+struct W8 {
+    float v[8];
+};
+
+// Weights [k0, k0+8) of the flat input, converted exactly to fp32.
+__device__ __forceinline__ W8 load8(const void *w, int dtype, int64_t k0) {
+    W8 r;
+    if (dtype == LOWBIT_DTYPE_F32) {
+        const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(w) + k0);
+        const float4 a = __ldcs(p), b = __ldcs(p + 1);
+        r.v[0] = a.x; r.v[1] = a.y; r.v[2] = a.z; r.v[3] = a.w;
+        r.v[4] = b.x; r.v[5] = b.y; r.v[6] = b.z; r.v[7] = b.w;
+    } else {
+        const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(
+            reinterpret_cast<const uint16_t *>(w) + k0));
+        const uint32_t words[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (dtype == LOWBIT_DTYPE_BF16) {
+                r.v[2 * i] = __uint_as_float(words[i] << 16);
+                r.v[2 * i + 1] = __uint_as_float(words[i] & 0xFFFF0000u);
+            } else {
+                r.v[2 * i] = __half2float(__ushort_as_half((uint16_t)(words[i] & 0xFFFFu)));
+                r.v[2 * i + 1] = __half2float(__ushort_as_half((uint16_t)(words[i] >> 16)));
+            }
+        }
+    }
+    return r;
+}
+
+// fp16 scale: rounded toward +inf of fl64(fl64(mx - z) / qmax).
+__device__ __forceinline__ uint16_t scale_bits(float mx, float z, float qmax) {
+    const uint16_t lo = __half_as_ushort(__float2half_ru(__fdiv_rd(__fsub_rd(mx, z), qmax)));
+    const uint16_t hi = __half_as_ushort(__float2half_ru(__fdiv_ru(__fsub_ru(mx, z), qmax)));
+    if (lo == hi) return lo;
+    const double t = ((double)mx - (double)z) / (double)qmax;
+    // Directed rounding to fp16 through fp32 in the same direction equals
+    // directed rounding to fp16 directly: every fp16 is an fp32.
+    return __half_as_ushort(__float2half_ru(__double2float_ru(t)));
+}
+
+// Code of one weight: clamp(rint(fl64(fl64(v - z) / s)), 0, qmax).
+__device__ __forceinline__ uint32_t code_of(float v, float z, float s, float inv_s, float qmax) {
+    const float r = __fmul_rn(__fsub_rn(v, z), inv_s);
+    float q = rintf(r);
+    if (fabsf(__fsub_rn(r, floorf(r)) - 0.5f) < 1.0f / 1024.0f)
+        q = (float)rint(((double)v - (double)z) / (double)s);
+    return (uint32_t)fminf(fmaxf(q, 0.0f), qmax);
+}
+
+// GL = lanes per group (g / 8): 4, 8, 16 or 32.
+template <int BITS, int GL>
+__global__ void __launch_bounds__(256)
+quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ packed,
+                uint16_t *__restrict__ scales, uint16_t *__restrict__ zeros, int64_t N, int K) {
+    constexpr int group = GL * 8;
+    constexpr float qmax = (float)((1 << BITS) - 1);
+    const int lane = threadIdx.x & 31;
+    const int G = K / group;
+    const int cpr = (K + kChunk - 1) / kChunk;               // chunks per row
+    const int64_t chunks = N * cpr;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+    const int64_t row_bytes = (int64_t)K * BITS / 8;
+
+    int64_t c = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (c >= chunks) return;                                 // whole warp leaves together
+    int64_t n = c / cpr;
+    int k = (int)(c - n * cpr) * kChunk + lane * 8;
+    W8 cur{};
+    if (k < K) cur = load8(w, dtype, n * K + k);
+    for (; c < chunks; c += warps) {
+        // Register double buffer: the next chunk's weights load while this one is coded.
+        const int64_t nc = c + warps;
+        int64_t n2 = 0;
+        int k2 = K;
+        W8 nxt{};
+        if (nc < chunks) {
+            n2 = nc / cpr;
+            k2 = (int)(nc - n2 * cpr) * kChunk + lane * 8;
+            if (k2 < K) nxt = load8(w, dtype, n2 * K + k2);
+        }
+        // A group lies wholly inside or wholly outside the row (K % group == 0),
+        // so lanes past the row end only ever reduce among themselves.
+        float mn = cur.v[0], mx = cur.v[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+            mn = fminf(mn, cur.v[i]);
+            mx = fmaxf(mx, cur.v[i]);
+        }
+#pragma unroll
+        for (int o = 1; o < GL; o <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        // A zero minimum takes the sign of the group's first zero (the first
+        // minimum a left-to-right scan meets).
+        if (__any_sync(0xffffffffu, mn == 0.0f)) {
+            uint32_t key = 0xFFFFFFFFu;                       // (position << 1) | sign
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (cur.v[i] == 0.0f)
+                    key = min(key, ((uint32_t)(lane * 8 + i) << 1) |
+                                       (__float_as_uint(cur.v[i]) >> 31));
+#pragma unroll
+            for (int o = 1; o < GL; o <<= 1)
+                key = min(key, __shfl_xor_sync(0xffffffffu, key, o));
+            if (mn == 0.0f) mn = (key & 1u) ? -0.0f : 0.0f;
+        }
+        if (k < K) {
+            const uint16_t zh = __half_as_ushort(__float2half_rd(mn));
+            const float z = __half2float(__ushort_as_half(zh));
+            const bool flat = (mx == mn);
+            const uint16_t sh = flat ? (uint16_t)0x0400 : scale_bits(mx, z, qmax);
+            const float s = __half2float(__ushort_as_half(sh));
+            const float inv_s = __frcp_rn(s);
+            uint64_t octet = 0;
+            if (!flat) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    octet |= (uint64_t)code_of(cur.v[i], z, s, inv_s, qmax) << (BITS * i);
+            }
+            uint8_t *dst = packed + n * row_bytes + (int64_t)(k / 8) * BITS;
+#pragma unroll
+            for (int i = 0; i < BITS; ++i) dst[i] = (uint8_t)(octet >> (8 * i));
+            if ((lane & (GL - 1)) == 0) {
+                const int64_t gi = n * G + k / group;
+                scales[gi] = sh;
+                zeros[gi] = zh;
+            }
+        }
+        cur = nxt;
+        n = n2;
+        k = k2;
+    }
+}
+
+// One resident wave: as many blocks as fit on the device at once (each warp
+// then strides over chunks), or fewer when there are fewer chunks.
+template <int BITS, int GL>
+cudaError_t launch_one(const void *w, int dtype, uint8_t *packed, uint16_t *scales,
+                       uint16_t *zeros, int64_t N, int K, cudaStream_t stream) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_kernel<BITS, GL>, 256, 0);
+    if (e != cudaSuccess) return e;
+    const int64_t chunks = N * ((K + kChunk - 1) / kChunk);
+    const int64_t want = (chunks + 7) / 8;
+    const int64_t wave = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+    const unsigned blocks = (unsigned)(want < wave ? want : wave);
+    quantize_kernel<BITS, GL><<<blocks, 256, 0, stream>>>(w, dtype, packed, scales, zeros, N, K);
+    return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t launch_bits(const void *w, int dtype, uint8_t *packed, uint16_t *scales,
+                        uint16_t *zeros, int64_t N, int K, int group, cudaStream_t stream) {
+    switch (group) {
+        case 32: return launch_one<BITS, 4>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 64: return launch_one<BITS, 8>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 128: return launch_one<BITS, 16>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 256: return launch_one<BITS, 32>(w, dtype, packed, scales, zeros, N, K, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const void *w, int dtype, uint8_t *packed, uint16_t *scales,
+                            uint16_t *zeros, int64_t N, int64_t K, int bits, int group,
+                            cudaStream_t stream) {
+    const int k = (int)K;
+    switch (bits) {
+        case 1: return launch_bits<1>(w, dtype, packed, scales, zeros, N, k, group, stream);
+        case 2: return launch_bits<2>(w, dtype, packed, scales, zeros, N, k, group, stream);
+        case 3: return launch_bits<3>(w, dtype, packed, scales, zeros, N, k, group, stream);
+        case 4: return launch_bits<4>(w, dtype, packed, scales, zeros, N, k, group, stream);
+        case 5: return launch_bits<5>(w, dtype, packed, scales, zeros, N, k, group, stream);
+        case 6: return launch_bits<6>(w, dtype, packed, scales, zeros, N, k, group, stream);
+        case 7: return launch_bits<7>(w, dtype, packed, scales, zeros, N, k, group, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace lowbit

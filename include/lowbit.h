@@ -73,6 +73,13 @@ typedef enum {
     LOWBIT_PATH_QMM = 2      /* tensor-core (tcgen05) matrix-matrix kernel, any M  */
 } lowbit_path;
 
+/* Element type of a floating-point input that is not fixed by the method. */
+typedef enum {
+    LOWBIT_DTYPE_F32 = 0,    /* IEEE binary32                                     */
+    LOWBIT_DTYPE_BF16 = 1,   /* bfloat16 bit patterns (uint16_t)                  */
+    LOWBIT_DTYPE_F16 = 2     /* IEEE binary16 bit patterns (uint16_t)             */
+} lowbit_dtype;
+
 /* Human-readable name of a status code.  Never NULL. */
 LOWBIT_API const char *lowbit_status_string(lowbit_status status);
 
@@ -101,6 +108,32 @@ LOWBIT_API lowbit_status lowbit_pack_weights(const uint8_t *codes, uint8_t *pack
  * `codes` the output (8-byte aligned). */
 LOWBIT_API lowbit_status lowbit_unpack_weights(const uint8_t *packed, uint8_t *codes,
                                     int64_t N, int64_t K, int bits, lowbit_stream_t stream);
+
+/* Quantise a floating-point weight matrix groupwise and write it in the
+ * packed layout, with its scales and zeros (the `_quantize` step of
+ * ao PR #2167, Summary, bullet 1, which produces N x num_groups scales and
+ * zeros; the pages do not define it, so this is the min/max asymmetric reading):
+ *     zero  = fp16 rounded toward -inf of min(w over the group)
+ *     scale = fp16 rounded toward +inf of (max - zero) / (2^bits - 1)
+ *     q     = clamp(round-half-to-even((w - zero) / scale), 0, 2^bits - 1)
+ * and a constant group (max == min) gets scale = 2^-14, q = 0.  Every
+ * decision is taken in fp64, so the outputs are fully determined by w.
+ * Then |w - (scale*q + zero)| <= scale/2 for every weight.
+ *   w        [N, K] of `dtype`, row-major, device, 16-byte aligned.
+ *            Values must be finite with magnitude at most 32752, so that a
+ *            group's zero and range fit fp16.
+ *   packed   [N, K*bits/8] uint8, device, written in full (any alignment).
+ *   scales   [N, K/group] fp16, row-major, device, 2-byte aligned.
+ *   zeros    [N, K/group] fp16, row-major, device, 2-byte aligned.
+ *   N >= 0, K > 0, group in {32, 64, 128, 256}, K % group == 0, bits in 1..7.
+ *   N == 0 is a valid empty call.  Outputs must not overlap w or each other.
+ * Errors: LOWBIT_EINVAL for a bad size, bit width, group, dtype, null or
+ * misaligned pointer; LOWBIT_EUNSUPPORTED on a device that is not sm_103;
+ * LOWBIT_ECUDA when the launch fails. */
+LOWBIT_API lowbit_status lowbit_quantize_weights(const void *w, lowbit_dtype dtype,
+                                      uint8_t *packed, uint16_t *scales, uint16_t *zeros,
+                                      int64_t N, int64_t K, int bits, int group,
+                                      lowbit_stream_t stream);
 
 /* The quantised linear layer (torchchat PR #1415; ao PR #2167 Summary
  * bullets 1-3; bias per ao issue #3446):

@@ -27,6 +27,7 @@ import numpy as np
 
 # Stream ids per tensor.
 STREAM_X, STREAM_CODES, STREAM_SCALE, STREAM_ZERO_U, STREAM_BIAS, STREAM_OUTLIER = 1, 2, 3, 4, 5, 6
+STREAM_WEIGHT = 7
 
 
 def rng(seed: int, stream: int, *key: int) -> np.random.Generator:
@@ -88,6 +89,18 @@ def make_scale_zero(seed: int, N: int, G: int, key: tuple = ()):
 
 def make_bias(seed: int, N: int, key: tuple = ()) -> np.ndarray:
     return f16_bits(rng(seed, STREAM_BIAS, N, *key).normal(0.0, 0.02, size=N))
+
+
+def make_weights(seed: int, N: int, K: int, key: tuple = ()) -> np.ndarray:
+    """Float weights [N, K] (float32) for the quantiser: N(0, 0.02), with one
+    row in 64 scaled by 8 and ceil(1% of K) columns by 4, so that groups span a
+    wide range of magnitudes."""
+    r = rng(seed, STREAM_WEIGHT, N, K, *key)
+    w = r.normal(0.0, 0.02, size=(N, K)).astype(np.float32)
+    if N > 0 and K > 0:
+        w[r.permutation(N)[: max(1, N // 64)]] *= 8.0
+        w[:, r.permutation(K)[: int(np.ceil(0.01 * K))]] *= 4.0
+    return w
 
 
 def make_layer(seed: int, M: int, K: int, N: int, bits: int, group: int,

@@ -115,6 +115,29 @@ def test_pack_empty_is_noop(lib):
     assert lib.lowbit_unpack_weights(None, None, 5, 0, 3, None) == 0
 
 
+# (w, dtype, packed, scales, zeros, N, K, bits, group); pointers are fake but
+# suitably aligned unless the case is about alignment: argument checks come
+# before any CUDA call, so none of these touches a device.
+_Q_OK = (4096, 0, 8192, 16384, 24576, 4, 256, 4, 64)
+
+
+@pytest.mark.parametrize("change", [
+    {7: 0}, {7: 8}, {8: 48}, {8: 512}, {6: 96}, {6: 0}, {5: -1}, {1: 3}, {1: -1},
+    {0: 0}, {2: 0}, {3: 0}, {4: 0}, {0: 4098}, {0: 4097, 1: 1}, {3: 16385}, {4: 24577},
+])
+def test_quantize_rejects_bad_arguments(lib, change):
+    args = list(_Q_OK)
+    for i, v in change.items():
+        args[i] = v
+    w, dt, p, s, z, N, K, bits, group = args
+    assert lib.lowbit_quantize_weights(w or None, dt, p or None, s or None, z or None,
+                                       N, K, bits, group, None) == EINVAL
+
+
+def test_quantize_empty_is_noop(lib):
+    assert lib.lowbit_quantize_weights(None, 1, None, None, None, 0, 256, 3, 128, None) == 0
+
+
 def test_wait_timeouts_rejects_null(lib):
     assert lib.lowbit_wait_timeouts(None, 0) == EINVAL
 
