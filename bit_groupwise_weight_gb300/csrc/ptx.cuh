@@ -118,6 +118,15 @@ __device__ __forceinline__ void ffma2(float2 &d, float2 a, float2 b, float2 c) {
     d = *reinterpret_cast<float2 *>(&r);
 }
 
+// (a & MASK) | bits with the mask as an immediate operand, so that only `bits`
+// needs a register (a constant shared by many calls stays in one register).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or_imm(uint32_t a, uint32_t bits) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(bits));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t bits) {
     // (a & mask) | bits in one LOP3 (immediate truth table 0xEA).
     uint32_t d;

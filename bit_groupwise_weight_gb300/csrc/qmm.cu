@@ -109,25 +109,25 @@ __device__ __forceinline__ uint32_t code_pair(const uint32_t (&w)[BITS]) {
     if constexpr (BITS == 4) {
         // One byte = the pair; byte * (1 + 2^12) puts its high nibble at bit 16.
         const uint32_t byte = ptx::prmt(w[I / 4], 0u, 0x4440u | (I % 4));
-        return ptx::lop3_and_or(byte * 0x1001u, 0x000F000Fu, kBf16Magic);
+        return ptx::and_or_imm<0x000F000Fu>(byte * 0x1001u, kBf16Magic);
     } else if constexpr (BITS == 2) {
         const uint32_t byte = ptx::prmt(w[I / 8], 0u, 0x4440u | ((I / 2) % 4));
         uint32_t v = byte * (1u + (1u << 14));
         if constexpr (I % 2) v >>= 4;
-        return ptx::lop3_and_or(v, 0x00030003u, kBf16Magic);
+        return ptx::and_or_imm<0x00030003u>(v, kBf16Magic);
     } else if constexpr (BITS == 1) {
         const uint32_t byte = ptx::prmt(w[I / 16], 0u, 0x4440u | ((I / 4) % 4));
         uint32_t v = byte * (1u + (1u << 15));
         if constexpr (I % 4) v >>= (I % 4) * 2;
-        return ptx::lop3_and_or(v, 0x00010001u, kBf16Magic);
+        return ptx::and_or_imm<0x00010001u>(v, kBf16Magic);
     } else if constexpr (2 * BITS <= 16 - BITS) {
         // 3 or 5 bits: the pair's 2b bits, spread by one multiply.
         const uint32_t c = stream_window<BITS, 2 * I * BITS>(w) & ((1u << (2 * BITS)) - 1u);
-        return ptx::lop3_and_or(c * (1u + (1u << (16 - BITS))), m | (m << 16), kBf16Magic);
+        return ptx::and_or_imm<m | (m << 16)>(c * (1u + (1u << (16 - BITS))), kBf16Magic);
     } else {
         const uint32_t lo = stream_window<BITS, 2 * I * BITS>(w);
         const uint32_t hi = stream_window<BITS, (2 * I + 1) * BITS - 16>(w);
-        return ptx::lop3_and_or(hi, m << 16, ptx::lop3_and_or(lo, m, kBf16Magic));
+        return ptx::and_or_imm<(m << 16)>(hi, ptx::and_or_imm<m>(lo, kBf16Magic));
     }
 }
 

@@ -232,7 +232,7 @@ __device__ __forceinline__ float window_code(const uint32_t (&cp)[Window<BITS>::
     constexpr int p = Window<BITS>::pos(J);
     constexpr uint32_t mask = ((1u << BITS) - 1u) << p;
     constexpr uint32_t expo = (uint32_t)(127 + 23 - p) << 23;
-    return __uint_as_float(ptx::lop3_and_or(cp[c], mask, expo));
+    return __uint_as_float(ptx::and_or_imm<mask>(cp[c], expo));
 }
 
 template <int BITS>

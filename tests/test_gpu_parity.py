@@ -109,6 +109,19 @@ def test_linear_edge_shapes(path, M, K, N, bits, group):
     check_close(y_to_f64(d.run(path)), _oracle_y(L), f"{(M, K, N, bits, group)}")
 
 
+@pytest.mark.parametrize("bits", range(1, 8))
+@pytest.mark.parametrize("M,K,N,group", [
+    (1, 2048, 10007, 64),       # three 16-row tiles per CTA, the last one ragged
+    (2, 3072, 5003, 128),       # two rows of x, K not a power of two
+    (1, 8192, 4999, 256),       # K split into chunks per stage
+    (2, 1024, 9001, 32),        # smallest K the decode kernel takes, g = 32
+])
+def test_linear_decode_tiles_and_chunks(bits, M, K, N, group):
+    L = synth.make_layer(60 + bits + K, M, K, N, bits, group, bias=(M == 2), outliers=(M == 2))
+    d = DeviceLayer(L)
+    check_close(y_to_f64(d.run(lb.PATH_QMV)), _oracle_y(L), f"{(M, K, N, bits, group)}")
+
+
 def test_linear_single_qmv_full():
     # K = N = 4096, M = 1, b = 4, g = 64, seed 0: every output.
     L = synth.make_layer(0, **synth.SINGLE_QMV)
