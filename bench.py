@@ -574,6 +574,24 @@ def run_profile_layer(spec: str, calls: int):
     return 0
 
 
+def run_profile_quantize(spec: str, calls: int):
+    """Quantise the gate+up weight (bf16) `calls` times, nothing timed: a fixed
+    workload for ncu captures.  spec = bits:group."""
+    import torch
+    import bit_groupwise_weight_gb300 as lb
+    from bit_groupwise_weight_gb300 import build as lbuild
+    lbuild.build()
+    bits, group = (int(v) for v in spec.split(":"))
+    K, N = synth.LLAMA_8B["gate_up"]
+    w = torch.from_numpy(synth.f32_to_bf16_bits(synth.make_weights(0, N, K)).view(np.int16))
+    w = w.view(torch.bfloat16).to("cuda:0")
+    for _ in range(calls):
+        lb.quantize_weights(w, bits, group)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_quantize": spec, "calls": calls}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -587,12 +605,16 @@ def main():
                     help="skip the secondary quantiser measurement")
     ap.add_argument("--profile-layer", default=None,
                     help="name:bits:M[:group] -- only call that layer (for ncu captures)")
+    ap.add_argument("--profile-quantize", default=None,
+                    help="bits:group -- only run the quantiser on the gate+up weight (for ncu captures)")
     ap.add_argument("--profile-calls", type=int, default=2)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.profile_layer:
         return run_profile_layer(args.profile_layer, args.profile_calls)
+    if args.profile_quantize:
+        return run_profile_quantize(args.profile_quantize, args.profile_calls)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -15,10 +15,11 @@
 //   - min and max are exact in fp32 (the inputs are fp32, bf16 or fp16);
 //   - the fp64 scale quotient lies between the fp32 quotients rounded down
 //     and up, so when both round up to the same fp16 that fp16 is the scale;
-//   - (w - zero) / scale in fp32 is within 2^-14 of the fp64 quotient (it is
-//     at most 2^7 and carries three roundings of 2^-24 relative), so its
-//     round-half-even agrees with fp64's unless it lies within that distance
-//     of a half-integer; codes closer than 2^-10 to one are recomputed in fp64.
+//   - (w - zero) / scale in fp32 differs from the fp64 quotient by less than
+//     3 * 2^-24 * 2^7 < 2^-15 (it is at most 2^7 and carries three roundings
+//     of 2^-24 relative), so its round-half-even agrees with fp64's unless it
+//     lies within that distance of a half-integer; codes within 2^-14 of one
+//     are recomputed in fp64.
 // The codes are written packed (contiguous, LSB-first, ao PR #2167 Summary
 // bullet 2).
 //
@@ -78,10 +79,30 @@ __device__ __forceinline__ uint16_t scale_bits(float mx, float z, float qmax) {
 __device__ __forceinline__ uint32_t code_of(float v, float z, float s, float inv_s, float qmax) {
     const float r = __fmul_rn(__fsub_rn(v, z), inv_s);
     float q = rintf(r);
-    if (fabsf(__fsub_rn(r, floorf(r)) - 0.5f) < 1.0f / 1024.0f)
+    // |r - q| is exact and at most 1/2; within 2^-14 of 1/2 the fp32 quotient
+    // cannot decide the rounding, fp64 does.
+    if (fabsf(__fsub_rn(r, q)) > 0.5f - 1.0f / 16384.0f)
         q = (float)rint(((double)v - (double)z) / (double)s);
     return (uint32_t)fminf(fmaxf(q, 0.0f), qmax);
 }
+
+// Lane-held octet of 8 b-bit codes: code i at bits [b*i, b*i+b) of (lo, hi).
+template <int BITS>
+struct Octet {
+    uint32_t lo = 0, hi = 0;
+    __device__ __forceinline__ void put(int i, uint32_t q) {
+        const int b = BITS * i;
+        if (b < 32) {
+            lo |= q << b;
+            if (b + BITS > 32) hi |= q >> (32 - b);
+        } else {
+            hi |= q << (b - 32);
+        }
+    }
+    __device__ __forceinline__ uint8_t byte(int i) const {
+        return (uint8_t)(i < 4 ? lo >> (8 * i) : hi >> (8 * (i - 4)));
+    }
+};
 
 // GL = lanes per group (g / 8): 4, 8, 16 or 32.
 template <int BITS, int GL>
@@ -99,21 +120,23 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
 
     int64_t c = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (c >= chunks) return;                                 // whole warp leaves together
+    // Chunk c is row c / cpr, chunk c % cpr of the row; the warp strides by
+    // `warps` chunks, i.e. dn rows and dc chunks with a carry.
+    const int64_t dn = warps / cpr;
+    const int dc = (int)(warps % cpr);
     int64_t n = c / cpr;
-    int k = (int)(c - n * cpr) * kChunk + lane * 8;
+    int kc = (int)(c - n * cpr);
+    int k = kc * kChunk + lane * 8;
     W8 cur{};
     if (k < K) cur = load8(w, dtype, n * K + k);
     for (; c < chunks; c += warps) {
         // Register double buffer: the next chunk's weights load while this one is coded.
-        const int64_t nc = c + warps;
-        int64_t n2 = 0;
-        int k2 = K;
+        int64_t n2 = n + dn;
+        int kc2 = kc + dc;
+        if (kc2 >= cpr) { kc2 -= cpr; ++n2; }
+        const int k2 = kc2 * kChunk + lane * 8;
         W8 nxt{};
-        if (nc < chunks) {
-            n2 = nc / cpr;
-            k2 = (int)(nc - n2 * cpr) * kChunk + lane * 8;
-            if (k2 < K) nxt = load8(w, dtype, n2 * K + k2);
-        }
+        if (c + warps < chunks && k2 < K) nxt = load8(w, dtype, n2 * K + k2);
         // A group lies wholly inside or wholly outside the row (K % group == 0),
         // so lanes past the row end only ever reduce among themselves.
         float mn = cur.v[0], mx = cur.v[0];
@@ -141,22 +164,26 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
                 key = min(key, __shfl_xor_sync(0xffffffffu, key, o));
             if (mn == 0.0f) mn = (key & 1u) ? -0.0f : 0.0f;
         }
+        const uint16_t zh = __half_as_ushort(__float2half_rd(mn));
+        const float z = __half2float(__ushort_as_half(zh));
+        const bool flat = (mx == mn);
+        // The first lane of each group computes the scale (two directed
+        // divisions); a group is an aligned run of GL lanes, so a shuffle
+        // hands it to the others.
+        uint32_t sh32 = 0x0400u;
+        if (!flat && (lane & (GL - 1)) == 0) sh32 = scale_bits(mx, z, qmax);
+        const uint16_t sh = (uint16_t)__shfl_sync(0xffffffffu, sh32, lane & ~(GL - 1));
         if (k < K) {
-            const uint16_t zh = __half_as_ushort(__float2half_rd(mn));
-            const float z = __half2float(__ushort_as_half(zh));
-            const bool flat = (mx == mn);
-            const uint16_t sh = flat ? (uint16_t)0x0400 : scale_bits(mx, z, qmax);
             const float s = __half2float(__ushort_as_half(sh));
             const float inv_s = __frcp_rn(s);
-            uint64_t octet = 0;
+            Octet<BITS> o;
             if (!flat) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    octet |= (uint64_t)code_of(cur.v[i], z, s, inv_s, qmax) << (BITS * i);
+                for (int i = 0; i < 8; ++i) o.put(i, code_of(cur.v[i], z, s, inv_s, qmax));
             }
             uint8_t *dst = packed + n * row_bytes + (int64_t)(k / 8) * BITS;
 #pragma unroll
-            for (int i = 0; i < BITS; ++i) dst[i] = (uint8_t)(octet >> (8 * i));
+            for (int i = 0; i < BITS; ++i) dst[i] = o.byte(i);
             if ((lane & (GL - 1)) == 0) {
                 const int64_t gi = n * G + k / group;
                 scales[gi] = sh;
@@ -165,6 +192,7 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
         }
         cur = nxt;
         n = n2;
+        kc = kc2;
         k = k2;
     }
 }
