@@ -84,6 +84,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
 }
 
+// Hint: fetch [src, src+bytes) into L2 (no data reaches the SM; L2 is
+// coherent, so it is safe before the data's producer has finished).  src
+// 16-byte aligned, bytes a multiple of 16; nothing is issued for bytes == 0.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    if (bytes == 0) return;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Byte permute: bytes of {b, a} picked by the selector nibbles.
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;

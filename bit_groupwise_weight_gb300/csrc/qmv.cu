@@ -376,7 +376,6 @@ qmv_stream_kernel(const StreamParams p) {
 
     // This CTA's passes [pass0, pass0 + npass).
     ptx::pdl_launch_dependents();
-    ptx::pdl_wait();            // inputs may come from the previous kernel in the stream
     const int c = blockIdx.x;
     const int ch0 = c * p.chunks_base + min(c, p.chunks_extra);
     const int nch = p.chunks_base + (c < p.chunks_extra ? 1 : 0);
@@ -391,7 +390,19 @@ qmv_stream_kernel(const StreamParams p) {
         }
         ptx::fence_mbar_init();
     }
+    if (tid == T && nstage > 0) {
+        // Ask L2 for the bytes of the first ring's worth of stages while the
+        // previous kernel in the stream may still be running (a hint: L2 is
+        // coherent, so data still being written is simply fetched again).
+        const int row0 = pass0 * p.R;
+        const int row1 = min((pass0 + min(S * p.SP, npass)) * p.R, p.N);
+        const uint32_t rows = (uint32_t)(row1 - row0);
+        ptx::bulk_prefetch_l2(p.w + (int64_t)row0 * p.row_bytes, (rows * p.row_bytes) & ~15u);
+        ptx::bulk_prefetch_l2(p.s + (int64_t)row0 * p.G, (rows * (uint32_t)p.G * 2u) & ~15u);
+        ptx::bulk_prefetch_l2(p.z + (int64_t)row0 * p.G, (rows * (uint32_t)p.G * 2u) & ~15u);
+    }
     __syncthreads();
+    ptx::pdl_wait();            // inputs may come from the previous kernel in the stream
 
     if (tid >= T) {
         // ---------------- producer warp: one elected lane issues the copies.
