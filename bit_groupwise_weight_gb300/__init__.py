@@ -9,6 +9,7 @@ if the compiled library is missing.
     packed = pack_weights(codes, bits)            # codes: uint8 [N, K] on cuda
     packed, scales, zeros = quantize_weights(w, bits=4, group=64)   # w: float [N, K]
     y = linear(x, packed, scales, zeros, bias, bits=4, group=64)
+    quantize_(model, bits=4, group=64)             # nn.Linear -> LowbitLinear, in place
 """
 from __future__ import annotations
 
@@ -28,9 +29,10 @@ from ._abi import (  # noqa: F401
     unpack_weights,
     wait_timeouts,
 )
+from .module import LowbitLinear, quantize_  # noqa: F401
 
 __all__ = [
-    "LowbitError", "PATH_AUTO", "PATH_QMM", "PATH_QMV", "abi", "linear", "linear_ptr",
+    "LowbitError", "LowbitLinear", "PATH_AUTO", "PATH_QMM", "PATH_QMV", "abi", "linear", "linear_ptr",
     "pack_weights", "packed_bytes", "quantize_weights", "select_path", "status_string", "unpack_weights",
-    "wait_timeouts",
+    "quantize_", "wait_timeouts",
 ]
