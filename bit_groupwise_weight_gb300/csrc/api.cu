@@ -63,7 +63,12 @@ lowbit_status check_linear_args(const uint16_t *x, const uint8_t *w, const uint1
 }
 
 // M at or below which the CUDA-core kernel is faster than the tensor-core one.
-constexpr int64_t kQmvMaxM = 2;
+// Measured on GB300 (Llama-3.1-8B qkv, gate+up and down, b = 4, g = 128): the
+// tensor-core kernel takes about the same time for any M up to 32 (its MMAs
+// stream 128 weight rows per instruction whatever N is), the CUDA-core kernel
+// time grows with M in steps of two rows; the CUDA-core kernel is faster on
+// every shape up to M = 6 and on some at M = 8.
+constexpr int64_t kQmvMaxM = 6;
 
 }  // namespace
 
