@@ -80,6 +80,9 @@ struct QmmParams {
     uint16_t *y;
     int M, N, K, G, log2g, TN, tmem_cols, nbuf, a_col, ktiles, lseg_log2, nseg;
     int pstages;            // depth of the packed-code ring
+    int ksplit;             // CTAs of a cluster that split K (1: no split)
+    int kt_unit;            // K tiles per split unit (a group spans whole units)
+    uint32_t recv_off;      // split-K: partial sums from the other CTAs (from base)
     uint32_t x_stage;       // TN * kBK * 2 bytes (two swizzle atoms of TN rows)
     uint32_t x_off, p_off, xs_off;   // offsets from the 1024-aligned base
     uint32_t idesc;         // tcgen05 instruction descriptor
@@ -148,6 +151,43 @@ __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t (&w)[BITS])
     }
 }
 
+// Final rows of one accumulating thread: y[m, n] = acc + bias for its chunks
+// (all of them when ks == 1; with split K only the chunks c with c % ks ==
+// rank, summing the partials of CTAs 0..ks-1 in order, its own from `acc`,
+// the others from `recv`).
+__device__ __forceinline__ void store_rows(const QmmParams &p, const float2 (&acc)[4][8], int h, int nchunk,
+                                           int n, int m0, int rank, int ks, const uint8_t *recv = nullptr,
+                                           int at = 0) {
+    const float bias = p.bias != nullptr ? half_bits_to_float(p.bias[n]) : 0.f;
+    const int J = (4 + ks - 1) / ks;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int ch = h + 2 * c;
+        if (ch >= nchunk || (ks > 1 && c % ks != rank)) continue;
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+        for (int src = 0; src < ks; ++src) {
+            if (src == rank || ks == 1) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += (j & 1) ? acc[c][j / 2].y : acc[c][j / 2].x;
+            } else {
+                const float4 *r = reinterpret_cast<const float4 *>(recv + ((src * J + c / ks) * 256 + at) * 64);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 t = r[j];
+                    v[4 * j] += t.x; v[4 * j + 1] += t.y; v[4 * j + 2] += t.z; v[4 * j + 3] += t.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int m = m0 + ch * 16 + j;
+            if (m < p.M) p.y[(int64_t)m * p.N + n] = float_to_bf16_bits(v[j] + bias);
+        }
+    }
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
@@ -160,7 +200,14 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
     ptx::pdl_launch_dependents();
     ptx::pdl_wait();            // inputs may come from the previous kernel in the stream
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kRowsOut;
+    // Split K: the ksplit CTAs of a cluster (consecutive blockIdx.x) share a row
+    // tile; CTA `rank` takes K tiles [kt0, kt0 + nkt), whole groups each.
+    const int ks = p.ksplit;
+    const int rank = ks > 1 ? (int)ptx::cluster_ctarank() : 0;
+    const int n0 = (blockIdx.x / ks) * kRowsOut;
+    const int units = p.ktiles / p.kt_unit;
+    const int kt0 = (units * rank / ks) * p.kt_unit;
+    const int nkt = (units * (rank + 1) / ks) * p.kt_unit - kt0;
     const int m0 = blockIdx.y * p.TN;
     constexpr uint32_t kPackedStage = kBM * (kBK * BITS / 8);
 
@@ -213,9 +260,10 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
             const uint32_t empty = lane == 0 ? p_empty : x_empty;
             const uint64_t pol = ptx::policy_evict_first();
             int issued = 0;
-            for (int kt = 0; kt < p.ktiles; ++kt, ++issued) {
-                const int st = kt % depth;
-                if (kt >= depth && !ptx::mbar_wait(empty + 8 * st, ((kt / depth) - 1) & 1, &g_qmm_timeouts))
+            for (int i = 0; i < nkt; ++i, ++issued) {
+                const int kt = kt0 + i;
+                const int st = i % depth;
+                if (i >= depth && !ptx::mbar_wait(empty + 8 * st, ((i / depth) - 1) & 1, &g_qmm_timeouts))
                     break;
                 const uint32_t bar = full + 8 * st;
                 if (lane == 0) {
@@ -235,7 +283,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
         // ---------------- MMA issuer.
         if (lane == 0) {
             bool ok = true;
-            for (int kt = 0; kt < p.ktiles && ok; ++kt) {
+            for (int kt = 0; kt < nkt && ok; ++kt) {          // kt relative to kt0 here
                 const int st = kt % kXStages, as = kt % kAStages;
                 ok = ptx::mbar_wait(x_full + 8 * st, (kt / kXStages) & 1, &g_qmm_timeouts) &&
                      ptx::mbar_wait(a_full + 8 * as, (kt / kAStages) & 1, &g_qmm_timeouts);
@@ -268,7 +316,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
         const int pr = q * 31 + lane;                    // packed row in the tile (lane 31: ones row)
         const uint32_t trow = ((uint32_t)(q * 32) << 16);
         bool ok = true;
-        for (int kt = 0; kt < p.ktiles && ok; ++kt) {
+        for (int kt = 0; kt < nkt && ok; ++kt) {              // kt relative to kt0 here
             const int st = kt % p.pstages, as = kt % kAStages;
             ok = ptx::mbar_wait(p_full + 8 * st, (kt / p.pstages) & 1, &g_qmm_timeouts);
             if (ok && kt >= kAStages)
@@ -319,10 +367,11 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
         const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
         // Scale and zero of segment seg+2 are fetched while segment seg is processed.
         const uint16_t *srow = p.s + (int64_t)nrow * p.G, *zrow = p.z + (int64_t)nrow * p.G;
-        auto seg_group = [&](int sg) { return min((sg << p.lseg_log2) >> p.log2g, p.G - 1); };
+        const int seg0 = kt0 * sps, nseg = nkt * sps;   // this CTA's segments
+        auto seg_group = [&](int sg) { return min(((seg0 + sg) << p.lseg_log2) >> p.log2g, p.G - 1); };
         uint16_t s0 = __ldg(srow + seg_group(0)), s1 = __ldg(srow + seg_group(1));
         uint16_t z0 = __ldg(zrow + seg_group(0)), z1 = __ldg(zrow + seg_group(1));
-        for (int seg = 0; seg < p.nseg; ++seg) {
+        for (int seg = 0; seg < nseg; ++seg) {
             const int b = seg % p.nbuf;
             const float sv = half_bits_to_float(s0);
             const float zv = half_bits_to_float(z0);
@@ -383,21 +432,38 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
                 __syncwarp();                            // xw is reused by the next pair of chunks
             }
         }
-        if (ok && row_ok) {
-            const float bias = p.bias != nullptr ? half_bits_to_float(p.bias[n]) : 0.f;
+        if (ks == 1) {
+            if (ok && row_ok) store_rows(p, acc, h, nchunk, n, m0, -1, 1);
+        } else {
+            // Split K: chunk c of every thread belongs to CTA c % ks of the
+            // cluster.  After every CTA of the cluster has left its pipeline,
+            // each sends the chunks it does not own to their owners' shared
+            // memory; after a second cluster barrier each owner adds the ks
+            // partial sums in rank order (the same order on every run) and
+            // stores the rows.
+            const int at = threadIdx.x - kFirstAccWarp * 32;           // 0..255
+            const int J = (4 + ks - 1) / ks;                           // owned chunks per CTA
+            ptx::cluster_sync();
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int ch = h + 2 * c;
-                if (ch < nchunk) {
+                const int ch = h + 2 * c, owner = c % ks;
+                if (ch < nchunk && owner != rank) {
+                    const uint32_t off = base + p.recv_off + (uint32_t)(((rank * J + c / ks) * 256 + at) * 64);
+                    const uint32_t dst = ptx::mapa_shared(off, (uint32_t)owner);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int m = m0 + ch * 16 + j;
-                        const float v = (j & 1) ? acc[c][j / 2].y : acc[c][j / 2].x;
-                        if (m < p.M) p.y[(int64_t)m * p.N + n] = float_to_bf16_bits(v + bias);
-                    }
+                    for (int j = 0; j < 8; j += 2)
+                        ptx::st_cluster_v4(dst + j * 8, acc[c][j].x, acc[c][j].y, acc[c][j + 1].x, acc[c][j + 1].y);
                 }
             }
+            ptx::cluster_sync();
+            if (ok && row_ok) store_rows(p, acc, h, nchunk, n, m0, rank, ks, smem + p.recv_off, at);
         }
+    }
+    if (ks > 1 && warp < kFirstAccWarp) {
+        // The other roles take part in the accumulators' two cluster barriers.
+        __syncwarp();
+        ptx::cluster_sync();
+        ptx::cluster_sync();
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -423,6 +489,49 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 std::atomic<int> g_smem_attr_set[8];
+
+int device_sm_count() {
+    static std::atomic<int> cached{0};
+    int v = cached.load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+    cached.store(sms, std::memory_order_relaxed);
+    return sms;
+}
+
+// Whether `clusters` clusters of ks CTAs (smem bytes each) can all be resident
+// at once.  Cached per (bit width, ks) for the last shared-memory size asked.
+template <int BITS>
+bool cluster_fits(int ks, uint32_t smem, int clusters) {
+    static std::atomic<uint64_t> cache[9];                // (smem << 32) | (max clusters + 1)
+    uint64_t c = cache[ks].load(std::memory_order_relaxed);
+    int maxc;
+    if (c != 0 && (uint32_t)(c >> 32) == smem) {
+        maxc = (int)(uint32_t)c - 1;
+    } else {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(ks * clusters);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = (unsigned)ks;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        maxc = 0;
+        if (cudaOccupancyMaxActiveClusters(&maxc, qmm_kernel<BITS>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            maxc = 0;
+        }
+        cache[ks].store(((uint64_t)smem << 32) | (uint32_t)(maxc + 1), std::memory_order_relaxed);
+    }
+    return maxc >= clusters;
+}
 
 template <int BITS>
 cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
@@ -481,8 +590,39 @@ cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, 
                              cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         g_smem_attr_set[BITS].store(1, std::memory_order_relaxed);
     }
-    const dim3 grid((N + kRowsOut - 1) / kRowsOut, (M + q.TN - 1) / q.TN);
-    cudaError_t e = launch_pdl(qmm_kernel<BITS>, grid, dim3(kThreads), smem, stream, xmap, wmap, q);
+    // Split K over a cluster when the row and batch tiles alone leave SMs idle:
+    // as many CTAs per tile as fill the SMs (at most 8, whole groups each),
+    // provided every cluster can be resident at once and the partial sums fit
+    // in the (by then idle) x and code rings.
+    const int ntiles = (N + kRowsOut - 1) / kRowsOut, mtiles = (M + q.TN - 1) / q.TN;
+    const int tiles = ntiles * mtiles;
+    q.kt_unit = std::max(1, group / kBK);
+    const int units = q.ktiles / q.kt_unit;
+    q.recv_off = q.x_off;
+    int ks = 1;
+    if (tiles < device_sm_count()) ks = std::min(std::min(8, device_sm_count() / tiles), units);
+    while (ks > 1) {
+        const uint32_t need = (uint32_t)(ks * ((4 + ks - 1) / ks)) * 256u * 64u;
+        if (q.recv_off + need <= smem - 1024u && cluster_fits<BITS>(ks, smem, tiles)) break;
+        --ks;
+    }
+    q.ksplit = ks;
+    const dim3 grid(ntiles * ks, mtiles);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)ks;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = ks > 1 ? 2 : 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, qmm_kernel<BITS>, xmap, wmap, q);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

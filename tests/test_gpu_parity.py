@@ -224,6 +224,18 @@ def test_qmm_every_bits_full_tiles(bits):
     check_close(y_to_f64(d.run(lb.PATH_QMM)), _oracle_y(L), f"qmm b={bits}")
 
 
+@pytest.mark.parametrize("M,name", [(128, "o"), (8, "down"), (128, "gate_up")])
+def test_qmm_split_k_is_deterministic(M, name):
+    # Small layers split K over a cluster; the partial sums are added in a
+    # fixed order, so repeated calls give identical bits.
+    K, N = synth.LLAMA_8B[name]
+    L = synth.make_layer(42, M, K, N, 4, 128, bias=True)
+    d = DeviceLayer(L)
+    y1 = d.run(lb.PATH_QMM)
+    y2 = d.run(lb.PATH_QMM)
+    assert torch.equal(y1, y2)
+
+
 def test_auto_path_picks_qmm_for_batches():
     assert lb.select_path(128, 4096, 4096, 4, 128) == lb.PATH_QMM
     assert lb.select_path(1, 4096, 4096, 4, 128) == lb.PATH_QMV
