@@ -62,13 +62,15 @@ lowbit_status check_linear_args(const uint16_t *x, const uint8_t *w, const uint1
     return LOWBIT_OK;
 }
 
-// M at or below which the CUDA-core kernel is faster than the tensor-core one.
-// Measured on GB300 (Llama-3.1-8B qkv, gate+up and down, b = 4, g = 128): the
-// tensor-core kernel takes about the same time for any M up to 32 (its MMAs
-// stream 128 weight rows per instruction whatever N is), the CUDA-core kernel
-// time grows with M in steps of two rows; the CUDA-core kernel is faster on
-// every shape up to M = 6 and on some at M = 8.
-constexpr int64_t kQmvMaxM = 6;
+// Crossover between the CUDA-core kernel (reads the weights once per two rows
+// of x) and the tensor-core kernel (time nearly independent of M up to 32),
+// measured on GB300 for the Llama-3.1-8B shapes at b = 4, g = 128.  The
+// tensor-core kernel splits K over a cluster when its row tiles are too few to
+// fill the GPU (N below ~9400 outputs); then it wins from M = 3 or 5, while
+// for wider layers the CUDA-core kernel stays ahead up to M = 6.
+constexpr int64_t kQmvMaxM = 2;
+constexpr int64_t kQmvMaxMWide = 6;
+constexpr int64_t kWideN = 9424;          // 76 row tiles of 124: half the SMs
 
 }  // namespace
 
@@ -129,7 +131,8 @@ lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int gr
         M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return LOWBIT_PATH_AUTO;
     // The tensor-core kernel needs K % 128 == 0; other shapes stay on the CUDA-core kernel.
-    return (M <= kQmvMaxM || K % 128 != 0) ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
+    if (K % 128 != 0 || M <= kQmvMaxM || (M <= kQmvMaxMWide && N >= kWideN)) return LOWBIT_PATH_QMV;
+    return LOWBIT_PATH_QMM;
 }
 
 lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *packed_w, const uint16_t *scales,

@@ -171,9 +171,10 @@ LOWBIT_API lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *pack
                                lowbit_path path, lowbit_stream_t stream);
 
 /* The kernel lowbit_linear runs for this problem: LOWBIT_PATH_QMV for small M
- * (decode) and for K not a multiple of 128, LOWBIT_PATH_QMM above the
- * measured crossover.  Host-only; never touches the GPU.  Returns
- * LOWBIT_PATH_AUTO for arguments lowbit_linear would reject. */
+ * (decode: M <= 2, or M <= 6 for layers with N >= 9424 outputs) and for K not
+ * a multiple of 128, LOWBIT_PATH_QMM above these measured crossovers.
+ * Host-only; never touches the GPU.  Returns LOWBIT_PATH_AUTO for arguments
+ * lowbit_linear would reject. */
 LOWBIT_API lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int group);
 
 /* Every wait inside the library's kernels (a stage of streamed weights, a

@@ -66,8 +66,11 @@ def test_select_path(lib):
     assert lb.select_path(1, 4096, 4096, 4, 64) == lb.PATH_QMV
     assert lb.select_path(0, 4096, 4096, 4, 64) == lb.PATH_QMV
     assert lb.select_path(128, 4096, 4096, 4, 64) == lb.PATH_QMM
-    assert lb.select_path(6, 4096, 4096, 4, 64) == lb.PATH_QMV      # measured crossover
-    assert lb.select_path(7, 4096, 4096, 4, 64) == lb.PATH_QMM
+    # Measured crossovers: narrow layers (qmm splits K) and wide ones.
+    assert lb.select_path(2, 4096, 4096, 4, 64) == lb.PATH_QMV
+    assert lb.select_path(3, 4096, 4096, 4, 64) == lb.PATH_QMM
+    assert lb.select_path(6, 4096, 28672, 4, 64) == lb.PATH_QMV
+    assert lb.select_path(7, 4096, 28672, 4, 64) == lb.PATH_QMM
     assert lb.select_path(128, 4096 + 64, 4096, 4, 64) == lb.PATH_QMV
     for bad in ((1, 4096, 4096, 0, 64), (1, 4096, 4096, 8, 64), (1, 4096, 4096, 4, 48),
                 (1, 4000, 4096, 4, 64), (1, 0, 4096, 4, 64), (-1, 4096, 4096, 4, 64)):
