@@ -282,30 +282,51 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
     } else if (warp == 1) {
         // ---------------- MMA issuer.
         if (lane == 0) {
+            // The tensor core queues only a few MMAs (an MMA completes about
+            // 400 cycles after it is issued), so any slow instruction between
+            // two MMAs idles it.  The stage's eight MMAs are therefore unrolled
+            // with operand addresses formed by adds, and ring and buffer
+            // indices advance by counters instead of divisions.
+            static_assert((kXStages & (kXStages - 1)) == 0 && (kAStages & (kAStages - 1)) == 0 && kBK == 128,
+                          "ring shapes");
+            const uint32_t idesc = p.idesc;
+            const int mmask = (lseg >> 4) - 1;            // MMAs per segment - 1 (7, 3 or 1)
+            const uint64_t xd0 = ptx::sw128_desc(x_base);
+            const uint64_t xd_stage = p.x_stage >> 4, xd_atom = p.x_stage >> 5;   // descriptor address units
+            int b = 0;                                    // TMEM buffer of the current segment
+            uint32_t tpar = 0;                            // parity of its t_empty wait (round r >= 1: (r - 1) & 1)
+            bool reuse = false;                           // buffers have all been used once
             bool ok = true;
             for (int kt = 0; kt < nkt && ok; ++kt) {          // kt relative to kt0 here
-                const int st = kt % kXStages, as = kt % kAStages;
+                const int st = kt & (kXStages - 1), as = kt & (kAStages - 1);
                 ok = ptx::mbar_wait(x_full + 8 * st, (kt / kXStages) & 1, &g_qmm_timeouts) &&
                      ptx::mbar_wait(a_full + 8 * as, (kt / kAStages) & 1, &g_qmm_timeouts);
                 if (!ok) break;
                 const uint32_t a_st = a_tmem + (uint32_t)(as * kACols);
-                const uint32_t x_st = x_base + st * p.x_stage;
-                for (int sg = 0; sg < sps && ok; ++sg) {
-                    const int seg = kt * sps + sg;
-                    const int b = seg % p.nbuf;
-                    if (seg >= p.nbuf)
-                        ok = ptx::mbar_wait(t_empty + 8 * b, ((seg / p.nbuf) - 1) & 1, &g_qmm_timeouts);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    const int kk0 = sg * (lseg / 16);
-                    for (int kk = kk0; kk < kk0 + lseg / 16; ++kk) {
-                        const uint32_t atom = kk >> 2, koff = (kk & 3) * 32;
-                        const uint64_t bd = ptx::sw128_desc(x_st + atom * (p.x_stage / 2) + koff);
-                        ptx::mma_f16_tmem_a(tmem + (uint32_t)(b * p.TN), a_st + (uint32_t)(kk * 8), bd, p.idesc,
-                                            kk != kk0);
+                const uint64_t xd = xd0 + (uint64_t)st * xd_stage;
+                uint32_t d = tmem;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    if ((kk & mmask) == 0) {
+                        if (reuse && !ptx::mbar_wait(t_empty + 8 * b, tpar, &g_qmm_timeouts)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        d = tmem + (uint32_t)(b * p.TN);
                     }
-                    ptx::mma_commit(t_full + 8 * b);
+                    ptx::mma_f16_tmem_a(d, a_st + (uint32_t)(kk * 8), xd + (uint64_t)((kk >> 2) * xd_atom + (kk & 3) * 2),
+                                        idesc, (kk & mmask) != 0);
+                    if ((kk & mmask) == mmask) {
+                        ptx::mma_commit(t_full + 8 * b);
+                        if (++b == p.nbuf) {
+                            b = 0;
+                            if (reuse) tpar ^= 1u;
+                            reuse = true;
+                        }
+                    }
                 }
+                if (!ok) break;
                 ptx::mma_commit(x_empty + 8 * st);
                 ptx::mma_commit(a_empty + 8 * as);
             }
