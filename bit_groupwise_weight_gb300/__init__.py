@@ -9,6 +9,7 @@ if the compiled library is missing.
     packed = pack_weights(codes, bits)            # codes: uint8 [N, K] on cuda
     packed, scales, zeros = quantize_weights(w, bits=4, group=64)   # w: float [N, K]
     y = linear(x, packed, scales, zeros, bias, bits=4, group=64)
+    h = linear_swiglu(x, packed_gate_up, scales, zeros, bias, bits=4, group=64)   # silu(gate) * up
     quantize_(model, bits=4, group=64)             # nn.Linear -> LowbitLinear, in place
 """
 from __future__ import annotations
@@ -21,6 +22,8 @@ from ._abi import (  # noqa: F401
     abi,
     linear,
     linear_ptr,
+    linear_swiglu,
+    linear_swiglu_ptr,
     pack_weights,
     packed_bytes,
     quantize_weights,
@@ -33,6 +36,7 @@ from .module import LowbitLinear, quantize_  # noqa: F401
 
 __all__ = [
     "LowbitError", "LowbitLinear", "PATH_AUTO", "PATH_QMM", "PATH_QMV", "abi", "linear", "linear_ptr",
+    "linear_swiglu", "linear_swiglu_ptr",
     "pack_weights", "packed_bytes", "quantize_weights", "select_path", "status_string", "unpack_weights",
     "quantize_", "wait_timeouts",
 ]

@@ -43,6 +43,8 @@ def _bind(lib):
     lib.lowbit_linear.restype = ci
     lib.lowbit_linear_ex.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, vp]
     lib.lowbit_linear_ex.restype = ci
+    lib.lowbit_linear_swiglu.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, vp]
+    lib.lowbit_linear_swiglu.restype = ci
     lib.lowbit_select_path.argtypes = [i64, i64, i64, ci, ci]
     lib.lowbit_select_path.restype = ci
     lib.lowbit_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32), ci]
@@ -184,6 +186,44 @@ def linear(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor, zeros:
                                   out.data_ptr(), M, K, N, bits, group, path, _stream(x.device)),
            "lowbit_linear")
     return out
+
+
+def linear_swiglu(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+                  bias: torch.Tensor | None, bits: int, group: int,
+                  out: torch.Tensor | None = None) -> torch.Tensor:
+    """silu(x @ W[:F]^T + bias[:F]) * (x @ W[F:]^T + bias[F:]) for a packed
+    weight of 2F rows (gate rows, then up rows).
+
+    x bf16 [M, K]; packed_w uint8 [2F, K*bits/8]; scales, zeros fp16
+    [2F, K/group]; bias fp16 [2F] or None.  Returns bf16 [M, F] (or writes ``out``).
+    """
+    M, K = x.shape
+    N = packed_w.shape[0]
+    if N % 2:
+        raise ValueError(f"packed_w must hold 2F rows (gate, then up), got {N}")
+    F = N // 2
+    _need(x, "x", torch.bfloat16, (M, K))
+    _need(packed_w, "packed_w", torch.uint8, (N, K * bits // 8))
+    G = K // group if group else 0
+    _need(scales, "scales", torch.float16, (N, G))
+    _need(zeros, "zeros", torch.float16, (N, G))
+    if bias is not None:
+        _need(bias, "bias", torch.float16, (N,))
+    if out is None:
+        out = torch.empty((M, F), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16, (M, F))
+    _check(abi().lowbit_linear_swiglu(x.data_ptr(), packed_w.data_ptr(), scales.data_ptr(),
+                                      zeros.data_ptr(), None if bias is None else bias.data_ptr(),
+                                      out.data_ptr(), M, K, F, bits, group, _stream(x.device)),
+           "lowbit_linear_swiglu")
+    return out
+
+
+def linear_swiglu_ptr(x: int, packed_w: int, scales: int, zeros: int, bias: int | None, y: int,
+                      M: int, K: int, F: int, bits: int, group: int, stream: int) -> None:
+    """The gated C call on raw device pointers (for CUDA-graph capture and timing loops)."""
+    _check(abi().lowbit_linear_swiglu(x, packed_w, scales, zeros, bias, y, M, K, F, bits, group, stream),
+           "lowbit_linear_swiglu")
 
 
 def linear_ptr(x: int, packed_w: int, scales: int, zeros: int, bias: int | None, y: int,

@@ -159,6 +159,18 @@ lowbit_status lowbit_linear(const uint16_t *x, const uint8_t *packed_w, const ui
                             LOWBIT_PATH_AUTO, stream);
 }
 
+lowbit_status lowbit_linear_swiglu(const uint16_t *x, const uint8_t *packed_w, const uint16_t *scales,
+                                   const uint16_t *zeros, const uint16_t *bias, uint16_t *y,
+                                   int64_t M, int64_t K, int64_t F, int bits, int group,
+                                   lowbit_stream_t stream) {
+    if (F < 0 || F > kMaxDim / 2) return LOWBIT_EINVAL;
+    lowbit_status st = check_linear_args(x, packed_w, scales, zeros, bias, y, M, K, 2 * F, bits, group);
+    if (st != LOWBIT_OK || M == 0 || F == 0) return st;
+    if ((st = check_device()) != LOWBIT_OK) return st;
+    return from_cuda(lowbit::launch_qmv_gated(x, packed_w, scales, zeros, bias, y, M, K, F, bits, group,
+                                              (cudaStream_t)stream));
+}
+
 lowbit_status lowbit_wait_timeouts(uint32_t *count, int reset) {
     if (count == nullptr) return LOWBIT_EINVAL;
     lowbit_status st = check_device();

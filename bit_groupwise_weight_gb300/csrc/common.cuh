@@ -50,6 +50,10 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// The gated activation of a gate/up projection pair: silu(a) * u, with
+// silu(a) = a / (1 + e^-a), in fp32 (expf from the CUDA math library).
+__device__ __forceinline__ float silu_mul(float a, float u) { return a / (1.0f + expf(-a)) * u; }
+
 // 128-bit streaming load that does not allocate in L1 (weights are read once).
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
     uint4 v;
@@ -122,6 +126,11 @@ cudaError_t launch_unpack(const uint8_t *packed, uint8_t *codes, int64_t N, int6
 cudaError_t launch_qmv(const uint16_t *x, const uint8_t *w, const uint16_t *scales,
                        const uint16_t *zeros, const uint16_t *bias, uint16_t *y, int64_t M,
                        int64_t K, int64_t N, int bits, int group, cudaStream_t stream);
+// Gated form: packed rows [0, F) are the gate projection and [F, 2F) the up
+// projection; y [M, F] = silu(gate) * up (bias, if any, has 2F entries).
+cudaError_t launch_qmv_gated(const uint16_t *x, const uint8_t *w, const uint16_t *scales,
+                             const uint16_t *zeros, const uint16_t *bias, uint16_t *y, int64_t M,
+                             int64_t K, int64_t F, int bits, int group, cudaStream_t stream);
 cudaError_t launch_quantize(const void *w, int dtype, uint8_t *packed, uint16_t *scales,
                             uint16_t *zeros, int64_t N, int64_t K, int bits, int group,
                             cudaStream_t stream);

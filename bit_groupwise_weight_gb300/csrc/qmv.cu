@@ -37,11 +37,15 @@ __global__ void __launch_bounds__(kQmvThreads)
 qmv_generic_kernel(const uint16_t *__restrict__ x, const uint8_t *__restrict__ w,
            const uint16_t *__restrict__ scales, const uint16_t *__restrict__ zeros,
            const uint16_t *__restrict__ bias, uint16_t *__restrict__ y,
-           int M, int K, int N, int log2g) {
+           int M, int K, int N, int log2g, int F) {
     const int KB = K >> 5;                       // 32-code blocks per row
     const int G = K >> log2g;                    // groups per row
     const int64_t rb = (int64_t)KB * 4 * BITS;   // packed bytes per row
+    // Plain: rows n0 .. n0+RT-1.  Gated (F > 0, N = 2F): slots r < RT/2 are the
+    // gate rows f0 + r, slots r >= RT/2 the matching up rows F + f0 + r - RT/2.
+    static_assert(RT % 2 == 0, "gated CTAs take row pairs");
     const int n0 = blockIdx.x * RT;
+    const int f0 = blockIdx.x * (RT / 2);
 
     float acc[RT][MT];
 #pragma unroll
@@ -56,7 +60,9 @@ qmv_generic_kernel(const uint16_t *__restrict__ x, const uint8_t *__restrict__ w
         const int gi = (kb << 5) >> log2g;
 #pragma unroll
         for (int r = 0; r < RT; ++r) {
-            const int n = min(n0 + r, N - 1);    // clamp: rows past N are computed, not stored
+            // Clamp: rows past the end are computed, not stored.
+            const int n = F == 0 ? min(n0 + r, N - 1)
+                                 : (r < RT / 2 ? 0 : F) + min(f0 + r % (RT / 2), F - 1);
             load_block<BITS>(w + (int64_t)n * rb + (int64_t)kb * 4 * BITS, wv[r]);
             sv[r] = half_bits_to_float(__ldg(scales + (int64_t)n * G + gi));
             zv[r] = half_bits_to_float(__ldg(zeros + (int64_t)n * G + gi));
@@ -117,15 +123,33 @@ qmv_generic_kernel(const uint16_t *__restrict__ x, const uint8_t *__restrict__ w
             if (lane == 0) red[warp][r * MT + m] = v;
         }
     __syncthreads();
-    if (threadIdx.x < RT * MT) {
-        const int r = threadIdx.x / MT, m = threadIdx.x % MT;
-        const int n = n0 + r;
-        if (n < N && m < M) {
-            float v = 0.f;
+    if (F == 0) {
+        if (threadIdx.x < RT * MT) {
+            const int r = threadIdx.x / MT, m = threadIdx.x % MT;
+            const int n = n0 + r;
+            if (n < N && m < M) {
+                float v = 0.f;
 #pragma unroll
-            for (int i = 0; i < kQmvThreads / 32; ++i) v += red[i][threadIdx.x];
-            if (bias != nullptr) v += half_bits_to_float(bias[n]);
-            y[(int64_t)m * N + n] = float_to_bf16_bits(v);
+                for (int i = 0; i < kQmvThreads / 32; ++i) v += red[i][threadIdx.x];
+                if (bias != nullptr) v += half_bits_to_float(bias[n]);
+                y[(int64_t)m * N + n] = float_to_bf16_bits(v);
+            }
+        }
+    } else if (threadIdx.x < (RT / 2) * MT) {
+        const int r = threadIdx.x / MT, m = threadIdx.x % MT;
+        const int f = f0 + r;
+        if (f < F && m < M) {
+            float a = 0.f, u = 0.f;
+#pragma unroll
+            for (int i = 0; i < kQmvThreads / 32; ++i) {
+                a += red[i][r * MT + m];
+                u += red[i][(r + RT / 2) * MT + m];
+            }
+            if (bias != nullptr) {
+                a += half_bits_to_float(bias[f]);
+                u += half_bits_to_float(bias[F + f]);
+            }
+            y[(int64_t)m * F + f] = float_to_bf16_bits(silu_mul(a, u));
         }
     }
 }
@@ -133,27 +157,28 @@ qmv_generic_kernel(const uint16_t *__restrict__ x, const uint8_t *__restrict__ w
 template <int BITS, int MT>
 cudaError_t launch_generic_mt(const uint16_t *x, const uint8_t *w, const uint16_t *s,
                               const uint16_t *z, const uint16_t *bias, uint16_t *y, int M, int K,
-                              int N, int log2g, cudaStream_t stream) {
+                              int N, int log2g, int F, cudaStream_t stream) {
     constexpr int RT = 4;
-    const int grid = (N + RT - 1) / RT;
+    const int grid = F == 0 ? (N + RT - 1) / RT : (F + RT / 2 - 1) / (RT / 2);
     qmv_generic_kernel<BITS, MT, RT><<<grid, kQmvThreads, 0, stream>>>(x, w, s, z, bias, y, M, K, N,
-                                                                      log2g);
+                                                                      log2g, F);
     return cudaGetLastError();
 }
 
 template <int BITS>
 cudaError_t launch_generic(const uint16_t *x, const uint8_t *w, const uint16_t *s,
                            const uint16_t *z, const uint16_t *bias, uint16_t *y, int64_t M, int K,
-                           int N, int log2g, cudaStream_t stream) {
+                           int N, int log2g, int F, cudaStream_t stream) {
     // Up to 4 rows of x per launch; larger M is processed in chunks of 4.
+    const int64_t ystride = F == 0 ? N : F;
     for (int64_t m0 = 0; m0 < M; m0 += 4) {
         const int mc = (int)((M - m0) < 4 ? (M - m0) : 4);
         const uint16_t *xc = x + m0 * K;
-        uint16_t *yc = y + m0 * N;
+        uint16_t *yc = y + m0 * ystride;
         cudaError_t e;
-        if (mc == 1) e = launch_generic_mt<BITS, 1>(xc, w, s, z, bias, yc, mc, K, N, log2g, stream);
-        else if (mc == 2) e = launch_generic_mt<BITS, 2>(xc, w, s, z, bias, yc, mc, K, N, log2g, stream);
-        else e = launch_generic_mt<BITS, 4>(xc, w, s, z, bias, yc, mc, K, N, log2g, stream);
+        if (mc == 1) e = launch_generic_mt<BITS, 1>(xc, w, s, z, bias, yc, mc, K, N, log2g, F, stream);
+        else if (mc == 2) e = launch_generic_mt<BITS, 2>(xc, w, s, z, bias, yc, mc, K, N, log2g, F, stream);
+        else e = launch_generic_mt<BITS, 4>(xc, w, s, z, bias, yc, mc, K, N, log2g, F, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -353,6 +378,7 @@ struct StreamParams {
     const uint16_t *bias;
     uint16_t *y;
     int N, K, KB, G, log2g, R, T, SP, stages;
+    int F;                            // gated: F outputs from rows [0, F) (gate) and [F, 2F) (up); 0: plain
     int chunk;                        // passes per split unit (keeps s/z copies 16-byte sized)
     int chunks, chunks_base, chunks_extra;   // split units in all; per CTA: base (+1 for the first extra)
     int total_passes;                 // ceil(N / R)
@@ -394,12 +420,17 @@ qmv_stream_kernel(const StreamParams p) {
         // Ask L2 for the bytes of the first ring's worth of stages while the
         // previous kernel in the stream may still be running (a hint: L2 is
         // coherent, so data still being written is simply fetched again).
-        const int row0 = pass0 * p.R;
-        const int row1 = min((pass0 + min(S * p.SP, npass)) * p.R, p.N);
-        const uint32_t rows = (uint32_t)(row1 - row0);
-        ptx::bulk_prefetch_l2(p.w + (int64_t)row0 * p.row_bytes, (rows * p.row_bytes) & ~15u);
-        ptx::bulk_prefetch_l2(p.s + (int64_t)row0 * p.G, (rows * (uint32_t)p.G * 2u) & ~15u);
-        ptx::bulk_prefetch_l2(p.z + (int64_t)row0 * p.G, (rows * (uint32_t)p.G * 2u) & ~15u);
+        const int pend = pass0 + min(S * p.SP, npass);
+        // Plain: one run of rows.  Gated: the gate run and the matching up run.
+        const int r0 = p.F == 0 ? pass0 * p.R : (pass0 >> 1) * p.R;
+        const int r1 = p.F == 0 ? min(pend * p.R, p.N) : min(((pend + 1) >> 1) * p.R, p.F);
+        const uint32_t rows = (uint32_t)(r1 - r0);
+        for (int h = 0; h < (p.F == 0 ? 1 : 2); ++h) {
+            const int row0 = h * p.F + r0;
+            ptx::bulk_prefetch_l2(p.w + (int64_t)row0 * p.row_bytes, (rows * p.row_bytes) & ~15u);
+            ptx::bulk_prefetch_l2(p.s + (int64_t)row0 * p.G, (rows * (uint32_t)p.G * 2u) & ~15u);
+            ptx::bulk_prefetch_l2(p.z + (int64_t)row0 * p.G, (rows * (uint32_t)p.G * 2u) & ~15u);
+        }
     }
     __syncthreads();
     ptx::pdl_wait();            // inputs may come from the previous kernel in the stream
@@ -413,17 +444,40 @@ qmv_stream_kernel(const StreamParams p) {
                 const int st = i % S;
                 if (i >= S && !ptx::mbar_wait(empty0 + 8 * st, ((i / S) - 1) & 1, &g_qmv_timeouts))
                     break;
-                const int row0 = (pass0 + i * p.SP) * p.R;
-                const int row1 = min((pass0 + min((i + 1) * p.SP, npass)) * p.R, p.N);
-                const uint32_t rows = (uint32_t)(row1 - row0);
-                const uint32_t wb = rows * p.row_bytes;
-                const uint32_t szb = rows * (uint32_t)p.G * 2u;
                 const uint32_t dst = sb + p.ring_off + st * p.stage_bytes;
                 const uint32_t bar = full0 + 8 * st;
-                ptx::mbar_arrive_expect_tx(bar, wb + 2 * szb);
-                ptx::bulk_g2s(dst, p.w + (int64_t)row0 * p.row_bytes, wb, bar, pol);
-                ptx::bulk_g2s(dst + p.w_stage, p.s + (int64_t)row0 * p.G, szb, bar, pol);
-                ptx::bulk_g2s(dst + p.w_stage + p.sz_stage, p.z + (int64_t)row0 * p.G, szb, bar, pol);
+                if (p.F == 0) {
+                    // The stage's passes are one contiguous run of rows.
+                    const int row0 = (pass0 + i * p.SP) * p.R;
+                    const int row1 = min((pass0 + min((i + 1) * p.SP, npass)) * p.R, p.N);
+                    const uint32_t rows = (uint32_t)(row1 - row0);
+                    const uint32_t wb = rows * p.row_bytes;
+                    const uint32_t szb = rows * (uint32_t)p.G * 2u;
+                    ptx::mbar_arrive_expect_tx(bar, wb + 2 * szb);
+                    ptx::bulk_g2s(dst, p.w + (int64_t)row0 * p.row_bytes, wb, bar, pol);
+                    ptx::bulk_g2s(dst + p.w_stage, p.s + (int64_t)row0 * p.G, szb, bar, pol);
+                    ptx::bulk_g2s(dst + p.w_stage + p.sz_stage, p.z + (int64_t)row0 * p.G, szb, bar, pol);
+                } else {
+                    // Gated: the stage's pass pairs (gate pass 2j, up pass 2j + 1)
+                    // cover gate rows [f0, f1) and up rows [F + f0, F + f1).  Each
+                    // run is one copy: gate rows fill slots [0, SP/2) of the stage,
+                    // up rows slots [SP/2, SP).
+                    const int f0 = ((pass0 + i * p.SP) >> 1) * p.R;
+                    const int f1 = min(((pass0 + min((i + 1) * p.SP, npass)) >> 1) * p.R, p.F);
+                    const uint32_t rows = (uint32_t)(f1 - f0);
+                    const uint32_t wb = rows * p.row_bytes;
+                    const uint32_t szb = rows * (uint32_t)p.G * 2u;
+                    const uint32_t half = (uint32_t)(p.SP / 2);
+                    ptx::mbar_arrive_expect_tx(bar, 2u * (wb + 2u * szb));
+                    for (int h = 0; h < 2; ++h) {
+                        const int64_t row0 = (int64_t)h * p.F + f0;
+                        const uint32_t wd = dst + (uint32_t)h * half * (uint32_t)p.R * p.row_bytes;
+                        const uint32_t sd = dst + p.w_stage + (uint32_t)h * half * (uint32_t)(p.R * p.G) * 2u;
+                        ptx::bulk_g2s(wd, p.w + row0 * p.row_bytes, wb, bar, pol);
+                        ptx::bulk_g2s(sd, p.s + row0 * p.G, szb, bar, pol);
+                        ptx::bulk_g2s(sd + p.sz_stage, p.z + row0 * p.G, szb, bar, pol);
+                    }
+                }
             }
             // Do not leave while this thread's last copies may still be landing.
             for (int i = max(0, issued - S); i < issued; ++i)
@@ -468,6 +522,11 @@ qmv_stream_kernel(const StreamParams p) {
     const uint32_t wstep = (uint32_t)T * (4 * BITS);         // weights of one pass
     const uint32_t szstep = (uint32_t)p.R * p.G * 2u;       // scales of one pass
     const uint32_t w_own = (uint32_t)tid * (4 * BITS);
+    // Offsets from a pass pair's first pass to the next pair and to its second pass.
+    const bool gated = p.F != 0;
+    const uint32_t w_pair = gated ? wstep : 2u * wstep, sz_pair = gated ? szstep : 2u * szstep;
+    const uint32_t w_odd = gated ? (uint32_t)(p.SP / 2) * wstep : wstep;
+    const uint32_t sz_odd = gated ? (uint32_t)(p.SP / 2) * szstep : szstep;
     const uint32_t sz_own = (uint32_t)(rr * p.G + gi) * 2u;
 
     // The output this thread finishes in every batch, if any: pass fj of the
@@ -487,7 +546,25 @@ qmv_stream_kernel(const StreamParams p) {
         float *rb = red + (batch & 1) * (NW * V);
         rb[warp * V + lane] = ws;
         ptx::named_sync(1, T);
-        if (finisher) {
+        if (p.F != 0) {
+            // Gated: finisher (pair fj, row slot fr, m) combines passes 2fj and 2fj + 1.
+            if (tid < (P / 2) * p.R * M) {
+                const int lp = batch * P + 2 * fj;
+                const int f = ((pass0 + lp) >> 1) * p.R + fr;
+                if (lp < npass && f < p.F) {
+                    float a = 0.f, u = 0.f;
+                    for (int w2 = fr * wpr; w2 < (fr + 1) * wpr; ++w2) {
+                        a += rb[w2 * V + (2 * fj) * M + fm];
+                        u += rb[w2 * V + (2 * fj + 1) * M + fm];
+                    }
+                    if (p.bias != nullptr) {
+                        a += half_bits_to_float(p.bias[f]);
+                        u += half_bits_to_float(p.bias[p.F + f]);
+                    }
+                    p.y[(int64_t)fm * p.F + f] = float_to_bf16_bits(silu_mul(a, u));
+                }
+            }
+        } else if (finisher) {
             const int lp = batch * P + fj;
             const int row = (pass0 + lp) * p.R + fr;
             if (lp < npass && row < p.N) {
@@ -510,15 +587,18 @@ qmv_stream_kernel(const StreamParams p) {
             stage = ring + st * p.stage_bytes;
         }
         float v[S0];
-        const uint8_t *wbase = stage + sp * wstep + w_own;
-        const uint8_t *sbase = stage + p.w_stage + sp * szstep + sz_own;
+        // Slot of the stage's pass sp + u (sp is even): plain sp + u; gated
+        // (sp + u) / 2, plus SP/2 for an up pass (u odd).
+        const uint8_t *wbase = stage + (gated ? (sp >> 1) : sp) * wstep + w_own;
+        const uint8_t *sbase = stage + p.w_stage + (gated ? (sp >> 1) : sp) * szstep + sz_own;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             uint32_t wv[BITS];
-            lds_block<BITS>(wbase + u * wstep, wv);
-            const float sv = half_bits_to_float(*reinterpret_cast<const uint16_t *>(sbase + u * szstep));
-            const float zv =
-                half_bits_to_float(*reinterpret_cast<const uint16_t *>(sbase + p.sz_stage + u * szstep));
+            const uint32_t wo = (u >> 1) * w_pair + (u & 1) * w_odd;
+            const uint32_t so = (u >> 1) * sz_pair + (u & 1) * sz_odd;
+            lds_block<BITS>(wbase + wo, wv);
+            const float sv = half_bits_to_float(*reinterpret_cast<const uint16_t *>(sbase + so));
+            const float zv = half_bits_to_float(*reinterpret_cast<const uint16_t *>(sbase + p.sz_stage + so));
             float d[M];
             block_dot<BITS, M>(wv, xr, d);
 #pragma unroll
@@ -600,22 +680,25 @@ constexpr uint32_t kStageTarget = 12u * 1024u;
 
 template <int BITS, int M>
 StreamPlan plan_stream(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
-                       const uint16_t *bias, uint16_t *y, int K, int N, int group) {
+                       const uint16_t *bias, uint16_t *y, int K, int N, int group, int F) {
     StreamPlan pl;
     if (K % 1024 != 0 || K / 32 > stream_max_consumers<M>()) return pl;
     const int G = K / group;
     if (((int64_t)N * G) % 8 != 0) return pl;
+    if (F != 0 && G % 8 != 0) return pl;          // gated passes copy R*G fp16 values each
     if (!aligned16(w) || !aligned16(s) || !aligned16(z) || !aligned16(x)) return pl;
     StreamParams &q = pl.prm;
     q.x = x; q.w = w; q.s = s; q.z = z; q.bias = bias; q.y = y;
     q.N = N; q.K = K; q.KB = K / 32; q.G = G; q.log2g = __builtin_ctz((unsigned)group);
+    q.F = F;
     q.R = (M == 1) ? (256 + q.KB - 1) / q.KB : 256 / q.KB;
     q.T = q.R * q.KB;
     const uint32_t w_pass = (uint32_t)q.T * 4u * BITS;
     const uint32_t sz_pass = (uint32_t)q.R * G * 2u;
     // Scale/zero copies must be 16-byte multiples: a split unit of `chunk`
     // passes holds chunk*R*G fp16 values, a multiple of 8.
-    q.chunk = 8 / std::gcd(8, q.R * G);
+    // Gated: split units are gate/up pass pairs (each pass is copied on its own).
+    q.chunk = F != 0 ? 2 : 8 / std::gcd(8, q.R * G);
     const int U = stream_unroll<BITS>();
     const int step = std::lcm(q.chunk, U);
     int SP = std::max(1, (int)(kStageTarget / (w_pass + 2u * sz_pass)));
@@ -632,7 +715,7 @@ StreamPlan plan_stream(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
     pl.smem = q.ring_off + q.stages * q.stage_bytes;
     if (pl.smem > 200u * 1024u) return pl;
     pl.threads = q.T + 32;
-    q.total_passes = (N + q.R - 1) / q.R;
+    q.total_passes = F != 0 ? 2 * ((F + q.R - 1) / q.R) : (N + q.R - 1) / q.R;
     q.chunks = (q.total_passes + q.chunk - 1) / q.chunk;
     const int occ = stream_occupancy<BITS, M>(pl.threads, pl.smem);
     pl.grid = std::max(1, std::min(q.chunks, sm_count() * occ));
@@ -649,28 +732,31 @@ cudaError_t launch_stream(const StreamPlan &pl, cudaStream_t stream) {
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// F == 0: y = x W^T + bias, W with N rows.  F > 0 (N == 2F): the gated form,
+// y[m, f] = silu(g) * u with g, u the outputs of rows f and F + f.
 template <int BITS>
 cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
                         const uint16_t *bias, uint16_t *y, int64_t M, int K, int N, int group,
-                        cudaStream_t stream) {
+                        int F, cudaStream_t stream) {
     const int log2g = __builtin_ctz((unsigned)group);
+    const int64_t ys = F != 0 ? F : N;           // elements per row of y
     // Rows of x two at a time through the stream kernel when its conditions hold.
-    StreamPlan p1 = plan_stream<BITS, 1>(x, w, s, z, bias, y, K, N, group);
-    if (!p1.ok) return launch_generic<BITS>(x, w, s, z, bias, y, M, K, N, log2g, stream);
+    StreamPlan p1 = plan_stream<BITS, 1>(x, w, s, z, bias, y, K, N, group, F);
+    if (!p1.ok) return launch_generic<BITS>(x, w, s, z, bias, y, M, K, N, log2g, F, stream);
     for (int64_t m0 = 0; m0 < M; m0 += 2) {
         const int mc = (int)std::min<int64_t>(2, M - m0);
         cudaError_t e;
         if (mc == 1) {
-            StreamPlan pl = plan_stream<BITS, 1>(x + m0 * K, w, s, z, bias, y + m0 * N, K, N, group);
+            StreamPlan pl = plan_stream<BITS, 1>(x + m0 * K, w, s, z, bias, y + m0 * ys, K, N, group, F);
             e = launch_stream<BITS, 1>(pl, stream);
         } else {
-            StreamPlan pl = plan_stream<BITS, 2>(x + m0 * K, w, s, z, bias, y + m0 * N, K, N, group);
+            StreamPlan pl = plan_stream<BITS, 2>(x + m0 * K, w, s, z, bias, y + m0 * ys, K, N, group, F);
             if (pl.ok) {
                 e = launch_stream<BITS, 2>(pl, stream);
             } else {  // two rows of x that do not fit one CTA's registers: one launch each
                 for (int i = 0; i < 2 && (e = cudaSuccess) == cudaSuccess; ++i) {
                     StreamPlan p1r = plan_stream<BITS, 1>(x + (m0 + i) * K, w, s, z, bias,
-                                                          y + (m0 + i) * N, K, N, group);
+                                                          y + (m0 + i) * ys, K, N, group, F);
                     e = launch_stream<BITS, 1>(p1r, stream);
                     if (e != cudaSuccess) break;
                 }
@@ -693,20 +779,33 @@ uint32_t qmv_timeouts(bool reset) {
     return v;
 }
 
+namespace {
+cudaError_t launch_any(const uint16_t *x, const uint8_t *w, const uint16_t *scales,
+                       const uint16_t *zeros, const uint16_t *bias, uint16_t *y, int64_t M,
+                       int K, int N, int bits, int group, int F, cudaStream_t stream) {
+    switch (bits) {
+        case 1: return launch_bits<1>(x, w, scales, zeros, bias, y, M, K, N, group, F, stream);
+        case 2: return launch_bits<2>(x, w, scales, zeros, bias, y, M, K, N, group, F, stream);
+        case 3: return launch_bits<3>(x, w, scales, zeros, bias, y, M, K, N, group, F, stream);
+        case 4: return launch_bits<4>(x, w, scales, zeros, bias, y, M, K, N, group, F, stream);
+        case 5: return launch_bits<5>(x, w, scales, zeros, bias, y, M, K, N, group, F, stream);
+        case 6: return launch_bits<6>(x, w, scales, zeros, bias, y, M, K, N, group, F, stream);
+        case 7: return launch_bits<7>(x, w, scales, zeros, bias, y, M, K, N, group, F, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+}  // namespace
+
 cudaError_t launch_qmv(const uint16_t *x, const uint8_t *w, const uint16_t *scales,
                        const uint16_t *zeros, const uint16_t *bias, uint16_t *y, int64_t M,
                        int64_t K, int64_t N, int bits, int group, cudaStream_t stream) {
-    const int k = (int)K, n = (int)N;
-    switch (bits) {
-        case 1: return launch_bits<1>(x, w, scales, zeros, bias, y, M, k, n, group, stream);
-        case 2: return launch_bits<2>(x, w, scales, zeros, bias, y, M, k, n, group, stream);
-        case 3: return launch_bits<3>(x, w, scales, zeros, bias, y, M, k, n, group, stream);
-        case 4: return launch_bits<4>(x, w, scales, zeros, bias, y, M, k, n, group, stream);
-        case 5: return launch_bits<5>(x, w, scales, zeros, bias, y, M, k, n, group, stream);
-        case 6: return launch_bits<6>(x, w, scales, zeros, bias, y, M, k, n, group, stream);
-        case 7: return launch_bits<7>(x, w, scales, zeros, bias, y, M, k, n, group, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return launch_any(x, w, scales, zeros, bias, y, M, (int)K, (int)N, bits, group, 0, stream);
+}
+
+cudaError_t launch_qmv_gated(const uint16_t *x, const uint8_t *w, const uint16_t *scales,
+                             const uint16_t *zeros, const uint16_t *bias, uint16_t *y, int64_t M,
+                             int64_t K, int64_t F, int bits, int group, cudaStream_t stream) {
+    return launch_any(x, w, scales, zeros, bias, y, M, (int)K, (int)(2 * F), bits, group, (int)F, stream);
 }
 
 }  // namespace lowbit

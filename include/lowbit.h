@@ -170,6 +170,32 @@ LOWBIT_API lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *pack
                                int64_t M, int64_t K, int64_t N, int bits, int group,
                                lowbit_path path, lowbit_stream_t stream);
 
+/* Gate and up projections of a gated MLP fused into one decode call: with the
+ * packed matrix holding 2F rows -- rows [0, F) the gate projection, rows
+ * [F, 2F) the up projection, each quantised as for lowbit_linear --
+ *     a[m,f] = sum_k x[m,k] W[f,k]   + bias[f]
+ *     u[m,f] = sum_k x[m,k] W[F+f,k] + bias[F+f]
+ *     y[m,f] = silu(a[m,f]) * u[m,f],   silu(a) = a / (1 + e^-a),
+ * computed in fp32 and rounded once to bf16 (a and u are never rounded).
+ * This is the decode step the pages time (torchchat PR #1415 and ao PR #2167
+ * measure Llama token generation, whose MLP applies this activation to its
+ * gate and up projections); it saves one launch and one pass over a and u.
+ * It runs the CUDA-core matrix-vector kernels for every M (rows of x two at a
+ * time), so it is meant for decode-sized M.
+ *   x        [M, K] bf16, as for lowbit_linear.
+ *   packed_w [2F, K*bits/8], scales and zeros [2F, K/group], bias NULL or
+ *            [2F] fp16: layouts, alignment and ownership as for lowbit_linear
+ *            with N = 2F.
+ *   y        [M, F] bf16, device, 2-byte aligned, written in full.
+ *   F >= 0; every other size limit as for lowbit_linear.  M == 0 or F == 0 is
+ *   a valid empty call.
+ * Errors: as for lowbit_linear (LOWBIT_EINVAL also for F < 0). */
+LOWBIT_API lowbit_status lowbit_linear_swiglu(const uint16_t *x, const uint8_t *packed_w,
+                                   const uint16_t *scales, const uint16_t *zeros,
+                                   const uint16_t *bias, uint16_t *y,
+                                   int64_t M, int64_t K, int64_t F, int bits, int group,
+                                   lowbit_stream_t stream);
+
 /* The kernel lowbit_linear runs for this problem: LOWBIT_PATH_QMV for small M
  * (decode: M <= 2, or M <= 6 for layers with N >= 9424 outputs) and for K not
  * a multiple of 128, LOWBIT_PATH_QMM above these measured crossovers.

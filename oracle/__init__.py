@@ -16,6 +16,9 @@ Functions follow the pages' definitions:
 * ``linear`` / ``linear_rows`` -- y = x W^T + bias in fp64 (torchchat PR #1415
   "Add torchao mps ops": weight-only quantization, bit width 1..7, group
   size 32..256; ao issue #3446: bias).
+* ``silu_mul`` / ``linear_swiglu`` -- silu(gate) * up over a layer whose
+  first half of rows is the gate projection and second half the up
+  projection (the MLP of the Llama decode the pages time; written out here).
 * ``quantize`` -- a min/max asymmetric reference quantiser (the pages name a
   ``_quantize`` function without defining it; ao PR #2167 Summary bullet 1).
 """
@@ -78,8 +81,9 @@ def _bind(lib):
     lib.oracle_linear_rows.argtypes = [u16p, u8p, u16p, u16p, u16p, i64, i64, i64,
                                        ctypes.c_int, ctypes.c_int, i64p, i64, f64p, f64p]
     lib.oracle_quantize.argtypes = [f64p, i64, i64, ctypes.c_int, ctypes.c_int, u8p, u16p, u16p]
+    lib.oracle_silu_mul.argtypes = [f64p, i64, i64, f64p]
     for name in ("oracle_pack", "oracle_unpack", "oracle_dequant", "oracle_linear",
-                 "oracle_linear_rows", "oracle_quantize"):
+                 "oracle_linear_rows", "oracle_quantize", "oracle_silu_mul"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -179,6 +183,28 @@ class Oracle:
                                                 group, self._ptr(rows), rows.size, self._ptr(y),
                                                 self._ptr(tmp)), "linear_rows")
         return y
+
+    def silu_mul(self, y: np.ndarray) -> np.ndarray:
+        """fp64 h [M, F] = silu(y[:, :F]) * y[:, F:] for y [M, 2F]."""
+        y = np.ascontiguousarray(y, dtype=np.float64)
+        M, N = y.shape
+        if N % 2:
+            raise ValueError("silu_mul needs an even number of columns")
+        h = np.empty((M, N // 2), dtype=np.float64)
+        self._check(self.lib.oracle_silu_mul(self._ptr(y), M, N // 2, self._ptr(h)), "silu_mul")
+        return h
+
+    def linear_swiglu(self, x, packed, scales, zeros, bias, K: int, bits: int, group: int) -> np.ndarray:
+        """fp64 h [M, F] for a 2F-row layer (gate rows, then up rows)."""
+        return self.silu_mul(self.linear(x, packed, scales, zeros, bias, K, bits, group))
+
+    def linear_swiglu_rows(self, x, packed, scales, zeros, bias, K: int, bits: int, group: int,
+                           fs) -> np.ndarray:
+        """fp64 h [M, len(fs)] for the listed outputs f only."""
+        fs = np.asarray(fs, dtype=np.int64)
+        F = packed.shape[0] // 2
+        y = self.linear_rows(x, packed, scales, zeros, bias, K, bits, group, np.concatenate([fs, F + fs]))
+        return self.silu_mul(y)
 
     def quantize(self, w: np.ndarray, bits: int, group: int):
         """Returns (codes uint8 [N,K], scales uint16 fp16 bits [N,K/g], zeros ditto)."""

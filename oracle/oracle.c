@@ -348,6 +348,39 @@ int oracle_linear(const uint16_t *x, const uint8_t *packed, const uint16_t *scal
 }
 
 /* ------------------------------------------------------------------------ */
+/* Gated activation of a gate/up projection pair.  The pages time Llama     */
+/* token generation (torchchat PR #1415, ao PR #2167 decode tables), whose  */
+/* MLP multiplies silu of the gate projection by the up projection; the     */
+/* pages do not write it out, so the plain reading is used:                 */
+/*   h[m,f] = silu(a) * u,  a = y[m, f],  u = y[m, F + f],                   */
+/*   silu(a) = a / (1 + exp(-a)),                                           */
+/* on the unrounded fp64 outputs y [M, 2F] of a layer whose first F rows    */
+/* are the gate projection and last F rows the up projection.               */
+/* ------------------------------------------------------------------------ */
+int oracle_silu_mul(const double *y, int64_t M, int64_t F, double *h)
+{
+    if (M < 0 || F < 0)
+        return ORACLE_EINVAL;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t f = 0; f < F; ++f) {
+#ifdef PLANT_SILU_SWAP
+            double a = y[m * 2 * F + F + f];
+            double u = y[m * 2 * F + f];
+#else
+            double a = y[m * 2 * F + f];
+            double u = y[m * 2 * F + F + f];
+#endif
+#ifdef PLANT_SILU_SIGN
+            double e = exp(a);
+#else
+            double e = exp(-a);
+#endif
+            h[m * F + f] = a / (1.0 + e) * u;
+        }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Reference quantiser.  The pages name a `_quantize` function that produces */
 /* the codes and the N x num_groups scales and zeros (ao PR #2167, Summary,  */
 /* bullet 1) but do not define it.  Reading used here (min/max asymmetric):  */

@@ -24,6 +24,8 @@ from __future__ import annotations
 import json
 from pathlib import Path
 
+import math
+
 import numpy as np
 
 import synth
@@ -356,6 +358,47 @@ def pin_quantizer_constant_group(o):
     assert np.all(0.3 - zf < 2.0 ** -11)     # one fp16 ulp at 0.3 is 2^-12
 
 
+def pin_silu_closed_forms(o):
+    """sigma(ln 3) = 3/4 and sigma(-ln 3) = 1/4 exactly, so silu(+-ln 3) are
+    +-ln 3 * (3/4, 1/4); silu(0) = 0; the product is linear in u."""
+    l3 = math.log(3.0)
+    y = np.array([[l3, -l3, 0.0, 2.5, 1.0, 1.0, 7.0, -3.0]])   # gates | ups (F = 4)
+    h = o.silu_mul(y)
+    want = [l3 * 0.75 * 1.0, -l3 * 0.25 * 1.0, 0.0, 2.5 * (1.0 / (1.0 + math.exp(-2.5))) * -3.0]
+    assert h.shape == (1, 4)
+    np.testing.assert_allclose(h[0, :2], want[:2], rtol=1e-15)
+    assert h[0, 2] == 0.0
+    # Doubling u doubles h.
+    y2 = y.copy(); y2[0, 4:] *= 2.0
+    np.testing.assert_allclose(o.silu_mul(y2), 2.0 * h, rtol=1e-15)
+
+
+def pin_silu_odd_identity(o):
+    """silu(a) - silu(-a) = a for every a (sigma(a) + sigma(-a) = 1), and the
+    tails: silu(a) -> a for large a, -> 0 for very negative a."""
+    a = np.array([-30.0, -4.0, -0.5, 0.25, 1.0, 6.0, 30.0])
+    F = a.size
+    pos = o.silu_mul(np.concatenate([a, np.ones(F)])[None, :])[0]
+    neg = o.silu_mul(np.concatenate([-a, np.ones(F)])[None, :])[0]
+    np.testing.assert_allclose(pos - neg, a, rtol=1e-14, atol=1e-14)
+    assert abs(pos[-1] - 30.0) < 1e-11 and abs(pos[0]) < 1e-11
+
+
+def pin_silu_layout(o):
+    """h[m, f] takes its gate from column f and its up value from column F + f
+    of the same row m (not interleaved, not transposed): gates drawn from
+    {ln 3, -ln 3, 0}, whose silu values are closed forms, and distinct ups."""
+    M, F = 3, 5
+    l3 = math.log(3.0)
+    silu_of = {0: l3 * 0.75, 1: -l3 * 0.25, 2: 0.0}
+    pick = np.array([[(3 * m + 2 * f) % 3 for f in range(F)] for m in range(M)])
+    gates = np.choose(pick, [l3, -l3, 0.0])
+    ups = np.arange(1, M * F + 1, dtype=np.float64).reshape(M, F) * 1.5
+    h = o.silu_mul(np.concatenate([gates, ups], axis=1))
+    want = np.vectorize(silu_of.get)(pick) * ups
+    np.testing.assert_allclose(h, want, rtol=1e-15, atol=0)
+
+
 PINS = [
     pin_pack_golden, pin_pack_bigint, pin_pack_numpy, pin_roundtrip,
     pin_brute_force_single_code, pin_brute_force_identity, pin_code_masking,
@@ -363,4 +406,5 @@ PINS = [
     pin_linear_worked, pin_linear_integer_matmul, pin_linear_zero_only, pin_linear_one_group,
     pin_linear_bias_and_rows, pin_linear_numpy_matmul, pin_linearity, pin_dequant,
     pin_quantizer_invariant, pin_quantizer_constant_group,
+    pin_silu_closed_forms, pin_silu_odd_identity, pin_silu_layout,
 ]

@@ -34,7 +34,7 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for fn in ("lowbit_pack_weights", "lowbit_linear", "lowbit_unpack_weights",
                "lowbit_packed_bytes", "lowbit_status_string", "lowbit_linear_ex",
-               "lowbit_select_path", "lowbit_wait_timeouts"):
+               "lowbit_select_path", "lowbit_wait_timeouts", "lowbit_linear_swiglu"):
         assert fn in names
 
 
@@ -103,6 +103,29 @@ def test_linear_empty_is_noop(lib):
     assert call_linear(lib, M=0) == 0
     assert call_linear(lib, N=0) == 0
     assert call_linear(lib, M=0, x=0, w=0, s=0, z=0, y=0) == 0
+
+
+def call_swiglu(lib, **kw):
+    a = dict(LINEAR_ARGS, **kw)
+    F = a.get("F", 4)
+    return lib.lowbit_linear_swiglu(a["x"] or None, a["w"] or None, a["s"] or None, a["z"] or None,
+                                    a["bias"] or None, a["y"] or None, a["M"], a["K"], F, a["bits"],
+                                    a["group"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(bits=0), dict(bits=8), dict(group=16), dict(K=80), dict(K=0), dict(M=-1), dict(F=-1),
+    dict(F=1 << 30), dict(x=0), dict(w=0), dict(s=0), dict(z=0), dict(y=0), dict(x=8), dict(w=24),
+    dict(s=1), dict(z=3), dict(y=5), dict(bias=7),
+])
+def test_swiglu_rejects_bad_arguments(lib, kw):
+    assert call_swiglu(lib, **kw) == EINVAL
+
+
+def test_swiglu_empty_is_noop(lib):
+    assert call_swiglu(lib, M=0) == 0
+    assert call_swiglu(lib, F=0) == 0
+    assert call_swiglu(lib, F=0, x=0, w=0, s=0, z=0, y=0) == 0
 
 
 @pytest.mark.parametrize("args", [
