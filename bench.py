@@ -18,6 +18,9 @@ and zeros, more than the 129 MB L2, so every launch reads its weights cold.
              tensor-core kernel, TFLOP/s against the measured bf16 peak.
   quantize   the GPU quantiser on the gate+up weight (bf16, b = 4, g = 64),
              GB/s against the measured HBM peak.
+  swiglu_gate_up  the fused gate+up call (silu(gate) * up, F = 14336 outputs)
+             on the gate+up weights of the step, per bit width, beside the
+             plain linear on the same weight.
   cpu_baseline  the fp64 CPU oracle on a bounded sample of output rows.
 
 ``--impl reference`` times the CPU oracle instead (the method's plain
@@ -482,6 +485,26 @@ def run_ours(args):
         us = max(graph_us(with_call) - flush_us, 1e-2) / nrep
         per_layer.append({"layer": t["name"], "bits": t["b"], "K": t["K"], "N": t["N"],
                           "us": round(us, 3), "GBps": round(t["bytes"] / us / 1e3, 1), "_us": us})
+    # --- the fused gate+up call (silu(gate) * up) on the same gate+up weights ----
+    swiglu = []
+    if not args.no_swiglu:
+        for t in layers:
+            if t["name"] != "gate_up":
+                continue
+            F = t["N"] // 2
+            h = torch.empty((1, F), dtype=torch.bfloat16, device=dev)
+
+            def with_glu(t=t, h=h, F=F):
+                for i in range(nrep):
+                    flush.fill_(i)
+                    lb.linear_swiglu_ptr(t["x"].data_ptr(), t["w"].data_ptr(), t["s"].data_ptr(),
+                                         t["z"].data_ptr(), None, h.data_ptr(), 1, t["K"], F, t["b"],
+                                         GROUP, stream.cuda_stream)
+            us = max(graph_us(with_glu) - flush_us, 1e-2) / nrep
+            plain = next(p for p in per_layer if p["layer"] == "gate_up" and p["bits"] == t["b"])
+            nbytes = algorithmic_bytes(1, t["K"], t["N"], t["b"], GROUP) - 2 * F   # y holds F outputs
+            swiglu.append({"bits": t["b"], "K": t["K"], "F": F, "us": round(us, 3),
+                           "plain_linear_us": plain["us"], "GBps": round(nbytes / us / 1e3, 1)})
     del flush
     kern_us = sum(p.pop("_us") for p in per_layer)
     achieved = step_bytes / kern_us / 1e3
@@ -535,6 +558,12 @@ def run_ours(args):
         line["qmm_m128"] = qmm
     if quant is not None:
         line["quantize"] = quant
+    if swiglu:
+        line["swiglu_gate_up"] = {
+            "M": 1, "group": GROUP, "layers": swiglu,
+            "what": "lowbit_linear_swiglu: silu(gate) * up from the 8B gate+up weight in one call "
+                    "(F = 14336 outputs); plain_linear_us is lowbit_linear on the same weight",
+            "timing": "per call, L2 flushed, CUDA-graph differences"}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample, rows = calibrate_oracle(args.cpu_seconds)
@@ -602,6 +631,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-qmm", action="store_true", help="skip the secondary M=128 qmm measurement")
+    ap.add_argument("--no-swiglu", action="store_true",
+                    help="skip the secondary fused gate+up (silu * up) measurement")
     ap.add_argument("--no-quantize", action="store_true",
                     help="skip the secondary quantiser measurement")
     ap.add_argument("--profile-layer", default=None,

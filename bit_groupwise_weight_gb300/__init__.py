@@ -32,10 +32,10 @@ from ._abi import (  # noqa: F401
     unpack_weights,
     wait_timeouts,
 )
-from .module import LowbitLinear, quantize_  # noqa: F401
+from .module import LowbitGateUp, LowbitLinear, quantize_  # noqa: F401
 
 __all__ = [
-    "LowbitError", "LowbitLinear", "PATH_AUTO", "PATH_QMM", "PATH_QMV", "abi", "linear", "linear_ptr",
+    "LowbitError", "LowbitGateUp", "LowbitLinear", "PATH_AUTO", "PATH_QMM", "PATH_QMV", "abi", "linear", "linear_ptr",
     "linear_swiglu", "linear_swiglu_ptr",
     "pack_weights", "packed_bytes", "quantize_weights", "select_path", "status_string", "unpack_weights",
     "quantize_", "wait_timeouts",

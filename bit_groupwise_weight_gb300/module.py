@@ -7,8 +7,10 @@ torchao": the `UIntxWeightOnlyQuantizedLinear` module and the recursive
 which calls the per-bit-width pack op for every linear; the same issue asks for
 bias support) sit above the C ABI here: `LowbitLinear.from_linear` quantises
 and packs a layer's weight on the GPU (`lowbit_quantize_weights`) and
-`forward` calls `lowbit_linear`.  Only argument marshalling happens in Python;
-both steps run in the library's kernels.
+`forward` calls `lowbit_linear`.  `LowbitGateUp` holds a gated MLP's gate
+and up projections as one packed weight and calls `lowbit_linear_swiglu`.
+Only argument marshalling happens in Python; every step runs in the
+library's kernels.
 """
 from __future__ import annotations
 
@@ -79,6 +81,62 @@ class LowbitLinear(torch.nn.Module):
     def extra_repr(self) -> str:
         return (f"in_features={self.in_features}, out_features={self.out_features}, "
                 f"bits={self.bits}, group={self.group}, bias={self.bias is not None}")
+
+
+class LowbitGateUp(torch.nn.Module):
+    """silu(x @ Wg^T + bg) * (x @ Wu^T + bu): the gate and up projections of a
+    gated MLP held as one packed weight of 2F rows (gate rows, then up rows)
+    and run as one call (``lowbit_linear_swiglu``).
+
+    Buffers: ``packed`` uint8 [2F, in*bits/8], ``scales`` and ``zeros`` fp16
+    [2F, in/group], ``bias`` fp16 [2F] or None.  Inputs bf16 [..., in];
+    outputs bf16 [..., F].
+    """
+
+    def __init__(self, in_features: int, hidden_features: int, bits: int, group: int,
+                 bias: bool = False, device=None):
+        super().__init__()
+        self.inner = LowbitLinear(in_features, 2 * hidden_features, bits, group, bias=bias, device=device)
+        self.in_features, self.hidden_features = in_features, hidden_features
+
+    @classmethod
+    @torch.no_grad()
+    def from_linears(cls, gate: torch.nn.Linear, up: torch.nn.Linear, bits: int, group: int) -> "LowbitGateUp":
+        """Quantise two CUDA nn.Linear layers of the same shape into one gated
+        layer (the gate's and up's rows quantised group by group exactly as
+        LowbitLinear.from_linear would quantise each)."""
+        if gate.weight.shape != up.weight.shape:
+            raise ValueError(f"gate and up must have the same shape, got {tuple(gate.weight.shape)} "
+                             f"and {tuple(up.weight.shape)}")
+        if (gate.bias is None) != (up.bias is None):
+            raise ValueError("gate and up must both have a bias or both have none")
+        if not gate.weight.is_cuda or not up.weight.is_cuda:
+            raise ValueError("from_linears needs both layers on a CUDA device")
+        m = cls(gate.in_features, gate.out_features, bits, group, bias=gate.bias is not None,
+                device=gate.weight.device)
+        w = torch.cat([gate.weight.detach(), up.weight.detach()], dim=0).contiguous()
+        i = m.inner
+        _abi.quantize_weights(w, bits, group, i.packed, i.scales, i.zeros)
+        if gate.bias is not None:
+            i.bias.copy_(torch.cat([gate.bias.detach(), up.bias.detach()]))   # fp16, once
+        return m
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        if x.dtype != torch.bfloat16:
+            raise ValueError(f"LowbitGateUp takes bf16 inputs, got {x.dtype}")
+        if x.shape[-1] != self.in_features:
+            raise ValueError(f"expected inputs [..., {self.in_features}], got {tuple(x.shape)}")
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, self.in_features)
+        if not x2.is_contiguous():
+            raise ValueError("inputs must be contiguous in their last dimension")
+        i = self.inner
+        h = _abi.linear_swiglu(x2, i.packed, i.scales, i.zeros, i.bias, i.bits, i.group)
+        return h.reshape(*lead, self.hidden_features)
+
+    def extra_repr(self) -> str:
+        return (f"in_features={self.in_features}, hidden_features={self.hidden_features}, "
+                f"bits={self.inner.bits}, group={self.inner.group}, bias={self.inner.bias is not None}")
 
 
 def quantize_(model: torch.nn.Module, bits: int, group: int,

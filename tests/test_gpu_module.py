@@ -77,3 +77,31 @@ def test_three_dimensional_inputs_and_filter(orc):
     assert y0.shape == (2, 5, 768)
     flat = model[0](x.reshape(10, 1024))
     assert torch.equal(y0.reshape(10, 768), flat)
+
+
+@pytest.mark.parametrize("bits,group,bias", [(4, 64, True), (3, 128, False)])
+def test_gate_up_module_matches_oracle(orc, bits, group, bias):
+    """LowbitGateUp from two nn.Linear layers against the oracle's gated layer
+    built from the oracle's own quantisation of the stacked weights."""
+    K, F = 1024, 300
+    torch.manual_seed(5)
+    gate = torch.nn.Linear(K, F, bias=bias)
+    up = torch.nn.Linear(K, F, bias=bias)
+    ws = []
+    for i, lin in enumerate((gate, up)):
+        lin.weight.data = _bf16_tensor(synth.make_weights(8, F, K, key=(i, bits))).cpu()
+        ws.append(synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(lin.weight.detach().float().numpy()))
+                  .astype(np.float64))
+        if bias:
+            lin.bias.data = torch.from_numpy(synth.make_bias(8, F, key=(i,)).view(np.int16)).view(torch.float16)
+    gate, up = gate.cuda(), up.cuda()
+    m = lb.LowbitGateUp.from_linears(gate, up, bits, group)
+    x = _bf16_tensor(synth.bf16_bits_to_f32(synth.make_x(8, 2 * 3, K))).view(2, 3, K)
+    h = m(x)
+    assert h.shape == (2, 3, F) and h.dtype == torch.bfloat16
+    w64 = np.concatenate(ws, axis=0)
+    codes, s, z = orc.quantize(w64, bits, group)
+    b = None if not bias else torch.cat([gate.bias, up.bias]).detach().cpu().numpy().view(np.uint16)
+    x_bits = x.reshape(6, K).cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    ref = orc.linear_swiglu(x_bits, orc.pack(codes, bits), s, z, b, K, bits, group)
+    check_close(y_to_f64(h.reshape(6, F)), ref, f"gate_up module b={bits} g={group}")

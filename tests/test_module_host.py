@@ -51,3 +51,21 @@ def test_quantize_walks_the_tree_and_respects_the_filter():
     # on a CPU model that means a clear error from the first eligible layer.
     with pytest.raises(ValueError, match="CUDA"):
         lb.quantize_(model, 4, 32)
+
+
+def test_gate_up_buffers_and_checks():
+    m = lb.LowbitGateUp(256, 48, bits=3, group=64, bias=True, device="cpu")
+    sd = m.state_dict()
+    assert sd["inner.packed"].shape == (96, 256 * 3 // 8) and sd["inner.bias"].shape == (96,)
+    with pytest.raises(ValueError, match="bf16"):
+        m(torch.zeros(2, 256, dtype=torch.float32))
+    with pytest.raises(ValueError, match="256"):
+        m(torch.zeros(2, 128, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="CUDA"):
+        m(torch.zeros(2, 256, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="same shape"):
+        lb.LowbitGateUp.from_linears(torch.nn.Linear(128, 16), torch.nn.Linear(128, 32), 4, 64)
+    with pytest.raises(ValueError, match="bias"):
+        lb.LowbitGateUp.from_linears(torch.nn.Linear(128, 16), torch.nn.Linear(128, 16, bias=False), 4, 64)
+    with pytest.raises(ValueError, match="CUDA"):
+        lb.LowbitGateUp.from_linears(torch.nn.Linear(128, 16), torch.nn.Linear(128, 16), 4, 64)
