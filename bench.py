@@ -18,6 +18,9 @@ and zeros, more than the 129 MB L2, so every launch reads its weights cold.
              tensor-core kernel, TFLOP/s against the measured bf16 peak.
   quantize   the GPU quantiser on the gate+up weight (bf16, b = 4, g = 64),
              GB/s against the measured HBM peak.
+  int4wo_128 the int4wo-128 configuration (b = 4, g = 128) of the same linears
+             at M = 1 (per call, L2 flushed) and M = 128 (the qmm_m128
+             numbers), summed over the 8B model's 32 decoder layers.
   swiglu_gate_up  the fused gate+up call (silu(gate) * up, F = 14336 outputs)
              on the gate+up weights of the step, per bit width, beside the
              plain linear on the same weight.
@@ -505,6 +508,25 @@ def run_ours(args):
             nbytes = algorithmic_bytes(1, t["K"], t["N"], t["b"], GROUP) - 2 * F   # y holds F outputs
             swiglu.append({"bits": t["b"], "K": t["K"], "F": F, "us": round(us, 3),
                            "plain_linear_us": plain["us"], "GBps": round(nbytes / us / 1e3, 1)})
+    # --- the int4wo-128 configuration (b = 4, g = 128) at M = 1 ------------------
+    int4_m1 = []
+    if not args.no_int4wo:
+        for t in layers:
+            if t["b"] != 4:
+                continue
+            sc, zc = synth.make_scale_zero(0, t["N"], t["K"] // 128, (t["K"], 4, 128))
+            s128 = torch.from_numpy(sc.view(np.int16)).view(torch.float16).to(dev)
+            z128 = torch.from_numpy(zc.view(np.int16)).view(torch.float16).to(dev)
+
+            def with_int4(t=t, s128=s128, z128=z128):
+                for i in range(nrep):
+                    flush.fill_(i)
+                    lb.linear_ptr(t["x"].data_ptr(), t["w"].data_ptr(), s128.data_ptr(), z128.data_ptr(),
+                                  None, t["y"].data_ptr(), 1, t["K"], t["N"], 4, 128, stream.cuda_stream)
+            us = max(graph_us(with_int4) - flush_us, 1e-2) / nrep
+            nbytes = algorithmic_bytes(1, t["K"], t["N"], 4, 128)
+            int4_m1.append({"layer": t["name"], "K": t["K"], "N": t["N"], "us": round(us, 3),
+                            "GBps": round(nbytes / us / 1e3, 1)})
     del flush
     kern_us = sum(p.pop("_us") for p in per_layer)
     achieved = step_bytes / kern_us / 1e3
@@ -536,6 +558,21 @@ def run_ours(args):
     e2e_value = world * step_bytes / (e2e_ms / 1e3) / 1e9
 
     qmm = None if args.no_qmm else measure_qmm(torch, lb, dev, stream)
+    int4wo = None
+    if int4_m1:
+        # The 8B model has 32 decoder layers of these four linears.
+        stack1 = 32 * sum(r["us"] for r in int4_m1)
+        int4wo = {"bits": 4, "group": 128, "M1": {"layers": int4_m1, "stack_us": round(stack1, 1),
+                                                  "linear_tokens_per_s": round(1e6 / stack1, 1),
+                                                  "timing": "per call, L2 flushed, CUDA-graph differences"}}
+        if qmm is not None:
+            stack128 = 32 * sum(r["us"] for r in qmm["layers"])
+            int4wo["M128"] = {"layers": qmm["layers"], "stack_us": round(stack128, 1),
+                              "linear_tokens_per_s": round(128 * 1e6 / stack128, 1),
+                              "timing": qmm["timing"]}
+        int4wo["what"] = ("the int4wo-128 configuration (4-bit codes, groups of 128) on the Llama-3.1-8B "
+                          "linears; stack_us = 32 decoder layers x (qkv + o + gate_up + down), the linear "
+                          "layers' share of one decode step (no attention, norms, embeddings or lm_head)")
     quant = None if args.no_quantize else measure_quantize(torch, lb, dev, stream)
 
     line = {
@@ -558,6 +595,8 @@ def run_ours(args):
         line["qmm_m128"] = qmm
     if quant is not None:
         line["quantize"] = quant
+    if int4wo is not None:
+        line["int4wo_128"] = int4wo
     if swiglu:
         line["swiglu_gate_up"] = {
             "M": 1, "group": GROUP, "layers": swiglu,
@@ -631,6 +670,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-qmm", action="store_true", help="skip the secondary M=128 qmm measurement")
+    ap.add_argument("--no-int4wo", action="store_true",
+                    help="skip the secondary int4wo-128 (b = 4, g = 128) configuration")
     ap.add_argument("--no-swiglu", action="store_true",
                     help="skip the secondary fused gate+up (silu * up) measurement")
     ap.add_argument("--no-quantize", action="store_true",

@@ -189,6 +189,17 @@ def test_llama8b_decode_sweep(bits, name):
     _sampled_check(L, _rows(N, 48, bits), what=f"8B {name} b={bits}")
 
 
+@pytest.mark.parametrize("path", PATHS, ids=lambda p: PATH_IDS[p])
+@pytest.mark.parametrize("M", [1, 128])
+@pytest.mark.parametrize("name", list(synth.LLAMA_8B))
+def test_llama8b_int4wo_128(path, M, name):
+    # The int4wo-128 configuration (4-bit codes, groups of 128) of every 8B
+    # linear, at batch 1 and 128, through both kernels.
+    K, N = synth.LLAMA_8B[name]
+    L = synth.make_layer(12, M, K, N, 4, 128, bias=False, outliers=(M > 1))
+    _sampled_check(L, _rows(N, 24, M + 7), path=path, what=f"int4wo-128 {name} M={M}")
+
+
 @pytest.mark.parametrize("bits", [2, 3, 4, 6])
 @pytest.mark.parametrize("group", [32, 64, 128, 256])
 @pytest.mark.parametrize("model,name", [("3B", "qkv"), ("3B", "down"), ("1B", "gate_up"), ("1B", "o")])
