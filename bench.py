@@ -11,7 +11,10 @@ and zeros, more than the 129 MB L2, so every launch reads its weights cold.
              with all inputs resident in HBM; the step is replayed from a
              CUDA graph of 28 C-ABI calls.
   e2e        the same metric with every input copied from pinned host memory
-             and y copied back, through the public Python binding, per step.
+             and y copied back, through the public Python binding, per step
+             (the step's inputs in one pinned arena, copied in four chunks that
+             overlap the previous chunk's layers; host-to-device bandwidth on
+             this machine, ~210 GB/s, bounds it).
   roofline   the qmv kernel alone: per-layer time (CUDA graphs of flush + call
              minus flush alone), summed over the 28 layers.
   qmm_m128   the batched form: the same shapes at M = 128, b = 4, g = 128 on the
@@ -533,29 +536,73 @@ def run_ours(args):
     hbm_peak, tc_peak, peak_kind = measured_peaks()
 
     # --- e2e: host buffers through the public API --------------------------------
+    # A step's inputs live in one pinned host arena (each tensor 256-byte
+    # aligned) and are copied in E2E_CHUNKS large copies on a copy stream; the
+    # layers of chunk c run on the compute stream as soon as chunk c has landed,
+    # while chunk c + 1 is still in flight.  The outputs land in one device
+    # arena and come back in one copy.  Timed from the first copy to the end of
+    # the last.
     e2e_steps = max(1, min(args.steps, 10))
-    host = []
+    align = 256
+    offs, size = [], 0
     for t in layers:
-        host.append({k: t[k].cpu().pin_memory() for k in ("x", "w", "s", "z")}
-                    | {"y": torch.empty((1, t["N"]), dtype=torch.bfloat16).pin_memory()})
-    h2d = sum(sum(h[k].numel() * h[k].element_size() for k in ("x", "w", "s", "z")) for h in host)
-    d2h = sum(h["y"].numel() * 2 for h in host)
+        o = {}
+        for k in ("x", "w", "s", "z"):
+            o[k] = size
+            size += (t[k].numel() * t[k].element_size() + align - 1) // align * align
+        offs.append(o)
+    host_arena = torch.empty(size, dtype=torch.uint8).pin_memory()
+    dev_arena = torch.empty(size, dtype=torch.uint8, device=dev)
+    views = []
+    for t, o in zip(layers, offs):
+        v = {}
+        for k in ("x", "w", "s", "z"):
+            nb = t[k].numel() * t[k].element_size()
+            host_arena[o[k]:o[k] + nb].copy_(t[k].reshape(-1).view(torch.uint8).cpu())
+            v[k] = dev_arena[o[k]:o[k] + nb].view(t[k].dtype).view(t[k].shape)
+        views.append(v)
+    y_sizes = [t["N"] for t in layers]
+    y_dev = torch.empty(sum(y_sizes), dtype=torch.bfloat16, device=dev)
+    y_host = torch.empty(sum(y_sizes), dtype=torch.bfloat16).pin_memory()
+    y_views, yo = [], 0
+    for n in y_sizes:
+        y_views.append(y_dev[yo:yo + n].view(1, n))
+        yo += n
+    E2E_CHUNKS = 4
+    bounds = [round(i * len(layers) / E2E_CHUNKS) for i in range(E2E_CHUNKS + 1)]
+    copy_stream = torch.cuda.Stream(dev)
+    h2d = size
+    d2h = y_host.numel() * 2
     torch.cuda.synchronize(dev)
     dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    landed = [torch.cuda.Event() for _ in range(E2E_CHUNKS)]
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(e2e_steps):
-            for t, h in zip(layers, host):
-                for k in ("x", "w", "s", "z"):
-                    t[k].copy_(h[k], non_blocking=True)
-                lb.linear(t["x"], t["w"], t["s"], t["z"], None, t["b"], GROUP, out=t["y"])
-                h["y"].copy_(t["y"], non_blocking=True)
+            copy_stream.wait_stream(stream)           # the previous step is done with the arena
+            with torch.cuda.stream(copy_stream):
+                for c in range(E2E_CHUNKS):
+                    lo = offs[bounds[c]]["x"]
+                    hi = offs[bounds[c + 1]]["x"] if bounds[c + 1] < len(layers) else size
+                    dev_arena[lo:hi].copy_(host_arena[lo:hi], non_blocking=True)
+                    landed[c].record(copy_stream)
+            for c in range(E2E_CHUNKS):
+                stream.wait_event(landed[c])
+                for i in range(bounds[c], bounds[c + 1]):
+                    t, v = layers[i], views[i]
+                    lb.linear(v["x"], v["w"], v["s"], v["z"], None, t["b"], GROUP, out=y_views[i])
+            y_host.copy_(y_dev, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = dist.max(e0.elapsed_time(e1)) / e2e_steps
     e2e_value = world * step_bytes / (e2e_ms / 1e3) / 1e9
+    # The arena round trip must reproduce the device-resident results.
+    for i, t in enumerate(layers):
+        ref = lb.linear(t["x"], t["w"], t["s"], t["z"], None, t["b"], GROUP)
+        assert torch.equal(y_views[i], ref), f"e2e output of layer {i} differs"
+    del dev_arena, host_arena
 
     qmm = None if args.no_qmm else measure_qmm(torch, lb, dev, stream)
     int4wo = None
