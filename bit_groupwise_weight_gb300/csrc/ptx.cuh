@@ -138,6 +138,16 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads) {
 }
 
 // d = a * b + c on two fp32 lanes at once (a, b, c, d as 64-bit pairs).
+// Packed fp32 add: two lanes, one instruction.
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)),
+          "l"(*reinterpret_cast<unsigned long long *>(&b)));
+    return *reinterpret_cast<float2 *>(&r);
+}
+
 __device__ __forceinline__ void ffma2(float2 &d, float2 a, float2 b, float2 c) {
     unsigned long long r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;"

@@ -294,8 +294,7 @@ __device__ __forceinline__ void block_dot(const uint32_t (&w)[BITS], const XRegs
     }(std::make_integer_sequence<int, 16>{});
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-        const float2 a = make_float2((acc[m][0].x + acc[m][1].x) + (acc[m][2].x + acc[m][3].x),
-                                     (acc[m][0].y + acc[m][1].y) + (acc[m][2].y + acc[m][3].y));
+        const float2 a = ptx::fadd2(ptx::fadd2(acc[m][0], acc[m][1]), ptx::fadd2(acc[m][2], acc[m][3]));
         d[m] = (a.x + a.y) - xr.cx[m];
     }
 }
