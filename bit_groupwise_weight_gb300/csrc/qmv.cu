@@ -385,11 +385,30 @@ struct StreamParams {
     uint32_t w_stage, sz_stage;       // bytes of a full stage: weights, and scales (= zeros)
     uint32_t stage_bytes;             // w_stage + 2*sz_stage
     uint32_t red_off, ring_off;       // shared-memory offsets
+    uint32_t lut_off;                 // b = 1 lookup tables (table decode only)
 };
 
-template <int BITS, int M>
+// Table decode (b = 1, one row of x).  Each nibble of a block's word holds
+// codes 4j .. 4j+3, so sum_k x_k q_k over the block is the sum over j of
+// T_j[nibble j], where T_j[e] = sum of x_{4j+i} over the set bits i of e: 8
+// shared-memory lookups and adds per 32 codes instead of a float per code.
+// The tables depend only on x, so each CTA builds them once, laid out
+// [j][e][kb] (kb fastest): the 32 lanes of a warp hold consecutive blocks kb
+// and never share a bank.
+__device__ __forceinline__ float lut_dot(uint32_t w, const float *tb, int KB) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float t = tb[(j * 16 + (int)((w >> (4 * j)) & 15u)) * KB];
+        if (j & 1) s1 += t; else s0 += t;
+    }
+    return s0 + s1;
+}
+
+template <int BITS, int M, bool LUT = false>
 __global__ void __launch_bounds__(stream_max_consumers<M>() + 32)
 qmv_stream_kernel(const StreamParams p) {
+    static_assert(!LUT || (BITS == 1 && M == 1), "table decode: one-bit codes, one row of x");
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int V = 32;              // (pass, m) slots per batch
     constexpr int P = V / M;           // passes per batch
@@ -515,6 +534,28 @@ qmv_stream_kernel(const StreamParams p) {
         }(std::make_integer_sequence<int, 16>{});
         xr.cx[m] = cx;
     }
+    const float *lut = reinterpret_cast<const float *>(smem + p.lut_off) + kb;
+    if constexpr (LUT) {
+        // Row slot 0's threads build the tables of their block kb (x is the same
+        // for every row slot); everyone waits for them.
+        if (rr == 0) {
+            float *tw = reinterpret_cast<float *>(smem + p.lut_off) + kb;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float a = xr.x[0][2 * j].x, b = xr.x[0][2 * j].y;
+                const float c = xr.x[0][2 * j + 1].x, d = xr.x[0][2 * j + 1].y;
+                float t[16];
+                t[0] = 0.f; t[1] = a; t[2] = b; t[3] = a + b;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) t[4 + i] = t[i] + c;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) t[8 + i] = t[i] + d;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) tw[(j * 16 + e) * p.KB] = t[e];
+            }
+        }
+        ptx::named_sync(2, T);
+    }
 
     float *red = reinterpret_cast<float *>(smem + p.red_off);
     const uint8_t *ring = smem + p.ring_off;
@@ -599,7 +640,8 @@ qmv_stream_kernel(const StreamParams p) {
             const float sv = half_bits_to_float(*reinterpret_cast<const uint16_t *>(sbase + so));
             const float zv = half_bits_to_float(*reinterpret_cast<const uint16_t *>(sbase + p.sz_stage + so));
             float d[M];
-            block_dot<BITS, M>(wv, xr, d);
+            if constexpr (LUT) d[0] = lut_dot(wv[0], lut, p.KB);
+            else block_dot<BITS, M>(wv, xr, d);
 #pragma unroll
             for (int m = 0; m < M; ++m) v[u * M + m] = fmaf(sv, d[m], zv * xr.xs[m]);
         }
@@ -632,9 +674,9 @@ struct StreamPlan {
 
 bool aligned16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
 
-template <int BITS, int M>
+template <int BITS, int M, bool LUT>
 const void *stream_kernel_ptr() {
-    return reinterpret_cast<const void *>(&qmv_stream_kernel<BITS, M>);
+    return reinterpret_cast<const void *>(&qmv_stream_kernel<BITS, M, LUT>);
 }
 
 // Resident CTAs per SM for (bits, M, warps, shared-memory bucket of 8 KB),
@@ -643,15 +685,15 @@ const void *stream_kernel_ptr() {
 // first use.
 std::atomic<int> g_occ_cache[8][3][18][26];
 
-template <int BITS, int M>
+template <int BITS, int M, bool LUT>
 int stream_occupancy(int threads, uint32_t smem) {
     const int ti = threads / 32;
     const int si = (int)((smem + 8191u) / 8192u);
     if (ti >= 18 || si >= 26) return 1;
-    std::atomic<int> &slot = g_occ_cache[BITS][M][ti][si];
+    std::atomic<int> &slot = g_occ_cache[LUT ? 0 : BITS][M][ti][si];   // slot 0: the table-decode kernel
     int v = slot.load(std::memory_order_relaxed);
     if (v > 0) return v;
-    const void *fn = stream_kernel_ptr<BITS, M>();
+    const void *fn = stream_kernel_ptr<BITS, M, LUT>();
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, (size_t)si * 8192u) != cudaSuccess ||
@@ -676,12 +718,17 @@ int sm_count() {
 // Shared memory a CTA may fill with ring stages (two CTAs fit on an SM).
 constexpr uint32_t kRingBudget = 96u * 1024u;
 constexpr uint32_t kStageTarget = 12u * 1024u;
+// Table decode: ring stages limited to this so that the tables (16 K bytes
+// for K codes per row) and the ring of two CTAs share an SM.
+constexpr uint32_t kLutRingBudget = 40u * 1024u;
+constexpr int kLutMaxK = 4096;
 
-template <int BITS, int M>
+template <int BITS, int M, bool LUT = false>
 StreamPlan plan_stream(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
                        const uint16_t *bias, uint16_t *y, int K, int N, int group, int F) {
     StreamPlan pl;
     if (K % 1024 != 0 || K / 32 > stream_max_consumers<M>()) return pl;
+    if (LUT && K > kLutMaxK) return pl;
     const int G = K / group;
     if (((int64_t)N * G) % 8 != 0) return pl;
     if (F != 0 && G % 8 != 0) return pl;          // gated passes copy R*G fp16 values each
@@ -707,16 +754,18 @@ StreamPlan plan_stream(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
     q.w_stage = SP * w_pass;
     q.sz_stage = SP * sz_pass;
     q.stage_bytes = q.w_stage + 2u * q.sz_stage;
-    q.stages = (int)std::min<uint32_t>(kMaxStages, std::max<uint32_t>(2u, kRingBudget / q.stage_bytes));
+    const uint32_t budget = LUT ? kLutRingBudget : kRingBudget;
+    q.stages = (int)std::min<uint32_t>(kMaxStages, std::max<uint32_t>(2u, budget / q.stage_bytes));
     q.red_off = 16u * kMaxStages;
     const uint32_t red_bytes = 2u * (q.T / 32) * 32u * 4u;
     q.ring_off = (q.red_off + red_bytes + 127u) & ~127u;
-    pl.smem = q.ring_off + q.stages * q.stage_bytes;
+    q.lut_off = (q.ring_off + q.stages * q.stage_bytes + 127u) & ~127u;
+    pl.smem = q.lut_off + (LUT ? 8u * 16u * (uint32_t)q.KB * 4u : 0u);
     if (pl.smem > 200u * 1024u) return pl;
     pl.threads = q.T + 32;
     q.total_passes = F != 0 ? 2 * ((F + q.R - 1) / q.R) : (N + q.R - 1) / q.R;
     q.chunks = (q.total_passes + q.chunk - 1) / q.chunk;
-    const int occ = stream_occupancy<BITS, M>(pl.threads, pl.smem);
+    const int occ = stream_occupancy<BITS, M, LUT>(pl.threads, pl.smem);
     pl.grid = std::max(1, std::min(q.chunks, sm_count() * occ));
     q.chunks_base = q.chunks / pl.grid;
     q.chunks_extra = q.chunks % pl.grid;
@@ -724,9 +773,9 @@ StreamPlan plan_stream(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
     return pl;
 }
 
-template <int BITS, int M>
+template <int BITS, int M, bool LUT = false>
 cudaError_t launch_stream(const StreamPlan &pl, cudaStream_t stream) {
-    cudaError_t e = launch_pdl(qmv_stream_kernel<BITS, M>, dim3(pl.grid), dim3(pl.threads), pl.smem,
+    cudaError_t e = launch_pdl(qmv_stream_kernel<BITS, M, LUT>, dim3(pl.grid), dim3(pl.threads), pl.smem,
                                stream, pl.prm);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -746,8 +795,18 @@ cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, 
         const int mc = (int)std::min<int64_t>(2, M - m0);
         cudaError_t e;
         if (mc == 1) {
-            StreamPlan pl = plan_stream<BITS, 1>(x + m0 * K, w, s, z, bias, y + m0 * ys, K, N, group, F);
-            e = launch_stream<BITS, 1>(pl, stream);
+            bool done = false;
+            if constexpr (BITS == 1) {             // table decode when its tables fit
+                StreamPlan pt = plan_stream<1, 1, true>(x + m0 * K, w, s, z, bias, y + m0 * ys, K, N, group, F);
+                if (pt.ok) {
+                    e = launch_stream<1, 1, true>(pt, stream);
+                    done = true;
+                }
+            }
+            if (!done) {
+                StreamPlan pl = plan_stream<BITS, 1>(x + m0 * K, w, s, z, bias, y + m0 * ys, K, N, group, F);
+                e = launch_stream<BITS, 1>(pl, stream);
+            }
         } else {
             StreamPlan pl = plan_stream<BITS, 2>(x + m0 * K, w, s, z, bias, y + m0 * ys, K, N, group, F);
             if (pl.ok) {
