@@ -80,6 +80,12 @@ def measured_peaks():
 # Distributed plumbing (replicas; no collective on the data path).
 # ---------------------------------------------------------------------------
 
+def whole_job_gbs(world: int, step_bytes: int, steps: int, ms_total_max: float) -> float:
+    """Weak scaling: every rank streams step_bytes per step; the job's rate is
+    all ranks' bytes over the slowest rank's time."""
+    return world * step_bytes * steps / (ms_total_max / 1e3) / 1e9
+
+
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
         int(os.environ.get("LOCAL_RANK", "0"))
@@ -451,7 +457,7 @@ def run_ours(args):
     ms_total = ev0.elapsed_time(ev1)
     ms_total = dist.max(ms_total)
     ms_per_step = ms_total / args.steps
-    value = world * step_bytes * args.steps / (ms_total / 1e3) / 1e9
+    value = whole_job_gbs(world, step_bytes, args.steps, ms_total)
 
     # --- per-layer kernel time, cold L2 (roofline of the qmv kernel) -------------
     # CUDA-event timestamps are coarse on this platform (about 2 us), so each layer is
