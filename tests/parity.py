@@ -3,11 +3,10 @@ the tolerance check.
 
 Tolerance for bf16 outputs against the fp64 oracle (stated with the method's
 target): element-wise |y - y_ref| <= 2e-2 * (1 + |y_ref|), and relative
-Frobenius error ||y - y_ref|| / ||y_ref|| <= 5e-3.  The library accumulates in
-fp32 and rounds once to bf16 (relative error 2^-9 ~ 2e-3 per element), so both
-bounds leave room for fp32 summation order and, on the tensor-core path, for
-rounding each dequantised weight to bf16 (another ~2^-9 relative per weight,
-which averages out over K).
+Frobenius error ||y - y_ref|| / ||y_ref|| <= 5e-3.  The library multiplies the
+exact codes (on the tensor cores as bf16 128 + q), accumulates in fp32 and
+rounds once to bf16 (relative error 2^-9 ~ 2e-3 per element), so both bounds
+leave room for fp32 summation order and the final rounding.
 """
 from __future__ import annotations
 
