@@ -1,10 +1,14 @@
 // qmv.cu -- quantised matrix-vector product for decode (small M), on CUDA
 // cores with fp32 accumulation.  Two kernels:
 //   qmv_stream_kernel  -- the decode kernel (M <= 2, K % 1024 == 0): persistent
-//                         CTAs stream their rows through a TMA-bulk ring;
+//                         CTAs stream their rows through a TMA-bulk ring; for
+//                         one-bit codes and one row of x it decodes by table
+//                         lookup (lut_dot);
 //   qmv_generic_kernel -- any shape the library accepts (ragged N, K % 32 == 0,
 //                         any M in chunks of 4); used where the stream kernel's
 //                         alignment conditions do not hold.
+// Both also run the gated form (F > 0): rows [0, F) are a gate projection and
+// rows [F, 2F) the matching up projection, and the output is silu(gate) * up.
 //
 // Method: ao PR #2167 "metal lowbit kernels: qmv_fast optimization" (Summary,
 // bullets 1-3) describes a matrix-vector kernel over contiguous b-bit codes
