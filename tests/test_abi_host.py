@@ -176,3 +176,21 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(abi_mod, "library_path", lambda: tmp_path / "missing.so")
     with pytest.raises(ImportError):
         abi_mod.abi()
+
+
+def test_plain_c_client_links_and_runs(lib, tmp_path):
+    """A C program built against include/lowbit.h and linked to the shared
+    library (no Python in between) runs the host-side entry points."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    exe = tmp_path / "abi_host_check"
+    libdir = lbuild.LIB.parent
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Werror", "-I", str(ROOT / "include"),
+                    str(ROOT / "tests" / "c" / "abi_host_check.c"), "-o", str(exe),
+                    "-L", str(libdir), "-llowbit", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    assert "c abi ok" in out.stdout
