@@ -28,6 +28,7 @@ from ._abi import (  # noqa: F401
     packed_bytes,
     quantize_weights,
     select_path,
+    selftest_wait_timeout,
     status_string,
     unpack_weights,
     wait_timeouts,
@@ -37,6 +38,6 @@ from .module import LowbitGateUp, LowbitLinear, quantize_  # noqa: F401
 __all__ = [
     "LowbitError", "LowbitGateUp", "LowbitLinear", "PATH_AUTO", "PATH_QMM", "PATH_QMV", "abi", "linear", "linear_ptr",
     "linear_swiglu", "linear_swiglu_ptr",
-    "pack_weights", "packed_bytes", "quantize_weights", "select_path", "status_string", "unpack_weights",
+    "pack_weights", "packed_bytes", "quantize_weights", "select_path", "selftest_wait_timeout", "status_string", "unpack_weights",
     "quantize_", "wait_timeouts",
 ]

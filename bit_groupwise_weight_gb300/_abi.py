@@ -49,6 +49,8 @@ def _bind(lib):
     lib.lowbit_select_path.restype = ci
     lib.lowbit_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32), ci]
     lib.lowbit_wait_timeouts.restype = ci
+    lib.lowbit_selftest_wait_timeout.argtypes = [vp, vp]
+    lib.lowbit_selftest_wait_timeout.restype = ci
     return lib
 
 
@@ -89,6 +91,17 @@ def wait_timeouts(reset: bool = False) -> int:
     n = ctypes.c_uint32(0)
     _check(abi().lowbit_wait_timeouts(ctypes.byref(n), int(reset)), "lowbit_wait_timeouts")
     return int(n.value)
+
+
+def selftest_wait_timeout(gave_up: torch.Tensor) -> None:
+    """Enqueue the bounded-wait self-test: a kernel whose wait nothing completes
+    gives up after the wait limit (about one second), writes 1 to ``gave_up``
+    (a CUDA uint32/int32 tensor of one element) and counts one timeout."""
+    if not isinstance(gave_up, torch.Tensor) or not gave_up.is_cuda or gave_up.numel() != 1 \
+            or gave_up.element_size() != 4:
+        raise ValueError("gave_up must be a one-element 32-bit CUDA tensor")
+    _check(abi().lowbit_selftest_wait_timeout(gave_up.data_ptr(), _stream(gave_up.device)),
+           "lowbit_selftest_wait_timeout")
 
 
 def _stream(device) -> int:

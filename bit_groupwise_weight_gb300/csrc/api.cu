@@ -7,8 +7,34 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace {
+
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// arrives on, through the same helper every kernel uses.  After the helper's
+// limit the wait gives up, counts itself in g_selftest_timeouts and the kernel
+// returns; nothing faults and the context stays usable.
+__device__ unsigned int g_selftest_timeouts;
+
+__global__ void wait_selftest_kernel(uint32_t *gave_up) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = lowbit::ptx::smem_u32(&bar);
+    lowbit::ptx::mbar_init(b, 1);
+    lowbit::ptx::fence_mbar_init();
+    const bool ok = lowbit::ptx::mbar_wait(b, 0, &g_selftest_timeouts);   // phase 0 never completes
+    *gave_up = ok ? 0u : 1u;
+}
+
+uint32_t selftest_timeouts(bool reset) {
+    unsigned int v = 0;
+    cudaMemcpyFromSymbol(&v, g_selftest_timeouts, sizeof(v));
+    if (reset) {
+        const unsigned int zero = 0;
+        cudaMemcpyToSymbol(g_selftest_timeouts, &zero, sizeof(zero));
+    }
+    return v;
+}
 
 bool bits_ok(int bits) { return bits >= 1 && bits <= 7; }
 bool group_ok(int g) { return g == 32 || g == 64 || g == 128 || g == 256; }
@@ -176,8 +202,16 @@ lowbit_status lowbit_wait_timeouts(uint32_t *count, int reset) {
     lowbit_status st = check_device();
     if (st != LOWBIT_OK) return st;
     if (cudaDeviceSynchronize() != cudaSuccess) return LOWBIT_ECUDA;
-    *count = lowbit::qmv_timeouts(reset != 0) + lowbit::qmm_timeouts(reset != 0);
+    *count = lowbit::qmv_timeouts(reset != 0) + lowbit::qmm_timeouts(reset != 0) + selftest_timeouts(reset != 0);
     return cudaGetLastError() == cudaSuccess ? LOWBIT_OK : LOWBIT_ECUDA;
+}
+
+lowbit_status lowbit_selftest_wait_timeout(uint32_t *gave_up, lowbit_stream_t stream) {
+    if (gave_up == nullptr || !aligned(gave_up, 4)) return LOWBIT_EINVAL;
+    lowbit_status st = check_device();
+    if (st != LOWBIT_OK) return st;
+    wait_selftest_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(gave_up);
+    return from_cuda(cudaGetLastError());
 }
 
 }  // extern "C"

@@ -214,6 +214,16 @@ LOWBIT_API lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int b
  * fails (for instance after an earlier kernel fault). */
 LOWBIT_API lowbit_status lowbit_wait_timeouts(uint32_t *count, int reset);
 
+/* Self-test of the bounded waits: enqueues one single-thread kernel that waits,
+ * through the library's bounded-wait helper, on a barrier nothing completes.
+ * After the wait limit (about one second) it gives up, writes 1 to *gave_up
+ * and counts one timeout (seen by lowbit_wait_timeouts); the kernel then
+ * returns normally, so the device stays usable.
+ *   gave_up  device pointer to one uint32_t, 4-byte aligned, written by the kernel.
+ * Errors: LOWBIT_EINVAL for a NULL or misaligned pointer; LOWBIT_EUNSUPPORTED
+ * on a device that is not sm_103; LOWBIT_ECUDA when the launch fails. */
+LOWBIT_API lowbit_status lowbit_selftest_wait_timeout(uint32_t *gave_up, lowbit_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -170,6 +170,11 @@ def test_wait_timeouts_rejects_null(lib):
     assert lib.lowbit_wait_timeouts(None, 0) == EINVAL
 
 
+def test_wait_selftest_rejects_bad_pointers(lib):
+    assert lib.lowbit_selftest_wait_timeout(None, None) == EINVAL
+    assert lib.lowbit_selftest_wait_timeout(0x1002, None) == EINVAL   # not 4-byte aligned
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import bit_groupwise_weight_gb300._abi as abi_mod
     monkeypatch.setattr(abi_mod, "_lib", None)
