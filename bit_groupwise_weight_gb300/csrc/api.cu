@@ -113,8 +113,9 @@ const char *lowbit_status_string(lowbit_status status) {
 }
 
 size_t lowbit_packed_bytes(int64_t N, int64_t K, int bits) {
-    if (!bits_ok(bits) || N < 0 || K < 0 || (K * bits) % 8 != 0) return 0;
-    if (N > kMaxDim || K > kMaxDim) return 0;
+    // Range first, so that K * bits cannot overflow.
+    if (!bits_ok(bits) || N < 0 || K < 0 || N > kMaxDim || K > kMaxDim) return 0;
+    if ((K * bits) % 8 != 0) return 0;
     return (size_t)(N * (K * bits / 8));
 }
 

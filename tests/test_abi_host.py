@@ -53,6 +53,8 @@ def test_packed_bytes(lib):
     assert lb.packed_bytes(1, 32, 8) == 0
     assert lb.packed_bytes(-1, 32, 4) == 0
     assert lb.packed_bytes(0, 32, 4) == 0
+    assert lb.packed_bytes(1, 1 << 62, 7) == 0    # beyond the size limit, no overflow
+    assert lb.packed_bytes(1 << 40, 64, 4) == 0
 
 
 def test_status_strings(lib):
