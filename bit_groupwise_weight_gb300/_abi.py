@@ -100,8 +100,9 @@ def selftest_wait_timeout(gave_up: torch.Tensor) -> None:
     if not isinstance(gave_up, torch.Tensor) or not gave_up.is_cuda or gave_up.numel() != 1 \
             or gave_up.element_size() != 4:
         raise ValueError("gave_up must be a one-element 32-bit CUDA tensor")
-    _check(abi().lowbit_selftest_wait_timeout(gave_up.data_ptr(), _stream(gave_up.device)),
-           "lowbit_selftest_wait_timeout")
+    with torch.cuda.device(gave_up.device):
+        _check(abi().lowbit_selftest_wait_timeout(gave_up.data_ptr(), _stream(gave_up.device)),
+               "lowbit_selftest_wait_timeout")
 
 
 def _stream(device) -> int:
@@ -124,6 +125,16 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _device_of(*tensors) -> torch.device:
+    """The one device every given tensor (None entries skipped) lives on; the
+    C call is then made with that device current."""
+    dev = tensors[0].device
+    for t in tensors[1:]:
+        if t is not None and t.device != dev:
+            raise ValueError(f"all tensors must be on one device, got {dev} and {t.device}")
+    return dev
+
+
 def pack_weights(codes: torch.Tensor, bits: int, out: torch.Tensor | None = None) -> torch.Tensor:
     """codes uint8 [N, K] (one code per byte) -> packed uint8 [N, K*bits/8]."""
     N, K = codes.shape
@@ -131,8 +142,10 @@ def pack_weights(codes: torch.Tensor, bits: int, out: torch.Tensor | None = None
     if out is None:
         out = torch.empty((N, K * bits // 8), dtype=torch.uint8, device=codes.device)
     _need(out, "out", torch.uint8, (N, K * bits // 8))
-    _check(abi().lowbit_pack_weights(codes.data_ptr(), out.data_ptr(), N, K, bits,
-                                     _stream(codes.device)), "lowbit_pack_weights")
+    dev = _device_of(codes, out)
+    with torch.cuda.device(dev):
+        _check(abi().lowbit_pack_weights(codes.data_ptr(), out.data_ptr(), N, K, bits, _stream(dev)),
+               "lowbit_pack_weights")
     return out
 
 
@@ -142,8 +155,10 @@ def unpack_weights(packed: torch.Tensor, K: int, bits: int, out: torch.Tensor | 
     if out is None:
         out = torch.empty((N, K), dtype=torch.uint8, device=packed.device)
     _need(out, "out", torch.uint8, (N, K))
-    _check(abi().lowbit_unpack_weights(packed.data_ptr(), out.data_ptr(), N, K, bits,
-                                       _stream(packed.device)), "lowbit_unpack_weights")
+    dev = _device_of(packed, out)
+    with torch.cuda.device(dev):
+        _check(abi().lowbit_unpack_weights(packed.data_ptr(), out.data_ptr(), N, K, bits, _stream(dev)),
+               "lowbit_unpack_weights")
     return out
 
 
@@ -168,9 +183,11 @@ def quantize_weights(w: torch.Tensor, bits: int, group: int, packed: torch.Tenso
     _need(packed, "packed", torch.uint8, (N, K * bits // 8))
     _need(scales, "scales", torch.float16, (N, G))
     _need(zeros, "zeros", torch.float16, (N, G))
-    _check(abi().lowbit_quantize_weights(w.data_ptr(), _W_DTYPES[w.dtype], packed.data_ptr(),
-                                         scales.data_ptr(), zeros.data_ptr(), N, K, bits, group,
-                                         _stream(w.device)), "lowbit_quantize_weights")
+    dev = _device_of(w, packed, scales, zeros)
+    with torch.cuda.device(dev):
+        _check(abi().lowbit_quantize_weights(w.data_ptr(), _W_DTYPES[w.dtype], packed.data_ptr(),
+                                             scales.data_ptr(), zeros.data_ptr(), N, K, bits, group,
+                                             _stream(dev)), "lowbit_quantize_weights")
     return packed, scales, zeros
 
 
@@ -194,10 +211,12 @@ def linear(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor, zeros:
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _need(out, "out", torch.bfloat16, (M, N))
-    _check(abi().lowbit_linear_ex(x.data_ptr(), packed_w.data_ptr(), scales.data_ptr(),
-                                  zeros.data_ptr(), None if bias is None else bias.data_ptr(),
-                                  out.data_ptr(), M, K, N, bits, group, path, _stream(x.device)),
-           "lowbit_linear")
+    dev = _device_of(x, packed_w, scales, zeros, bias, out)
+    with torch.cuda.device(dev):
+        _check(abi().lowbit_linear_ex(x.data_ptr(), packed_w.data_ptr(), scales.data_ptr(),
+                                      zeros.data_ptr(), None if bias is None else bias.data_ptr(),
+                                      out.data_ptr(), M, K, N, bits, group, path, _stream(dev)),
+               "lowbit_linear")
     return out
 
 
@@ -225,10 +244,12 @@ def linear_swiglu(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor,
     if out is None:
         out = torch.empty((M, F), dtype=torch.bfloat16, device=x.device)
     _need(out, "out", torch.bfloat16, (M, F))
-    _check(abi().lowbit_linear_swiglu(x.data_ptr(), packed_w.data_ptr(), scales.data_ptr(),
-                                      zeros.data_ptr(), None if bias is None else bias.data_ptr(),
-                                      out.data_ptr(), M, K, F, bits, group, _stream(x.device)),
-           "lowbit_linear_swiglu")
+    dev = _device_of(x, packed_w, scales, zeros, bias, out)
+    with torch.cuda.device(dev):
+        _check(abi().lowbit_linear_swiglu(x.data_ptr(), packed_w.data_ptr(), scales.data_ptr(),
+                                          zeros.data_ptr(), None if bias is None else bias.data_ptr(),
+                                          out.data_ptr(), M, K, F, bits, group, _stream(dev)),
+               "lowbit_linear_swiglu")
     return out
 
 

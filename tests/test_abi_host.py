@@ -201,3 +201,12 @@ def test_plain_c_client_links_and_runs(lib, tmp_path):
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert out.returncode == 0, out.stderr
     assert "c abi ok" in out.stdout
+
+
+def test_binding_requires_one_device():
+    from types import SimpleNamespace
+    from bit_groupwise_weight_gb300 import _abi
+    a, b = SimpleNamespace(device="cuda:0"), SimpleNamespace(device="cuda:1")
+    assert _abi._device_of(a, None, a) == "cuda:0"
+    with pytest.raises(ValueError, match="one device"):
+        _abi._device_of(a, b)
