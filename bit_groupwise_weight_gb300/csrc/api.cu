@@ -203,7 +203,8 @@ lowbit_status lowbit_wait_timeouts(uint32_t *count, int reset) {
     lowbit_status st = check_device();
     if (st != LOWBIT_OK) return st;
     if (cudaDeviceSynchronize() != cudaSuccess) return LOWBIT_ECUDA;
-    *count = lowbit::qmv_timeouts(reset != 0) + lowbit::qmm_timeouts(reset != 0) + selftest_timeouts(reset != 0);
+    *count = lowbit::qmv_timeouts(reset != 0) + lowbit::mma_timeouts(reset != 0) + lowbit::qmm_timeouts(reset != 0) +
+             selftest_timeouts(reset != 0);
     return cudaGetLastError() == cudaSuccess ? LOWBIT_OK : LOWBIT_ECUDA;
 }
 

@@ -134,7 +134,16 @@ cudaError_t launch_qmv_gated(const uint16_t *x, const uint8_t *w, const uint16_t
 cudaError_t launch_quantize(const void *w, int dtype, uint8_t *packed, uint16_t *scales,
                             uint16_t *zeros, int64_t N, int64_t K, int bits, int group,
                             cudaStream_t stream);
+// The decode kernel on the warp-level tensor cores (qmv_mma.cuh), any M in
+// launches of up to 8 rows of x; F > 0: the gated form (N = 2F rows).  Returns
+// cudaErrorNotSupported, having launched nothing, for shapes it does not take
+// (K not a multiple of 256, K > 32768, F not a multiple of 16, x or the
+// packed weights not 16-byte aligned).
+cudaError_t launch_qmv_mma(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
+                           const uint16_t *bias, uint16_t *y, int64_t M, int64_t K, int64_t N, int bits, int group,
+                           int64_t F, cudaStream_t stream);
 // Bounded waits that gave up, per kernel file (device counters; reading syncs).
+uint32_t mma_timeouts(bool reset);
 uint32_t qmv_timeouts(bool reset);
 uint32_t qmm_timeouts(bool reset);
 // True when the tensor-core kernel handles this shape (K a multiple of 128,

@@ -790,6 +790,9 @@ template <int BITS>
 cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
                         const uint16_t *bias, uint16_t *y, int64_t M, int K, int N, int group,
                         int F, cudaStream_t stream) {
+    // The tensor-core decode kernel takes every shape it supports.
+    const cudaError_t em = launch_qmv_mma(x, w, s, z, bias, y, M, K, N, BITS, group, F, stream);
+    if (em != cudaErrorNotSupported) return em;
     const int log2g = __builtin_ctz((unsigned)group);
     const int64_t ys = F != 0 ? F : N;           // elements per row of y
     // Rows of x two at a time through the stream kernel when its conditions hold.

@@ -1,0 +1,179 @@
+// qmv_mma_host.cu -- host side of the warp-level tensor-core decode kernel
+// (qmv_mma.cuh): bit-width dispatch, the shared-memory padding model, and
+// per-device caches of the launch limits.
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "qmv_mma.cuh"
+
+namespace lowbit {
+namespace mma {
+
+#define LOWBIT_MMA_DECL(B)                                                                                  \
+    cudaError_t launch_b##B(const uint16_t *, const uint8_t *, const uint16_t *, const uint16_t *,          \
+                            const uint16_t *, uint16_t *, int64_t, int, int, int, int, cudaStream_t);       \
+    uint32_t timeouts_b##B(bool);
+LOWBIT_MMA_DECL(1)
+LOWBIT_MMA_DECL(2)
+LOWBIT_MMA_DECL(3)
+LOWBIT_MMA_DECL(4)
+LOWBIT_MMA_DECL(5)
+LOWBIT_MMA_DECL(6)
+LOWBIT_MMA_DECL(7)
+#undef LOWBIT_MMA_DECL
+
+namespace {
+
+// Shared-memory wavefronts of one pass of the consumers' weight reads for a
+// staged-row stride: lane 4 gid + t reads, for blocks beta = 0, 1, the b words
+// at row gid, byte (128 beta + 32 t) b / 8, with the widest aligned loads.
+int model_wavefronts(int bits, uint32_t stride) {
+    const int width = bits == 4 ? 16 : ((bits == 2 || bits == 6) ? 8 : 4);
+    const int per_phase = width == 16 ? 8 : (width == 8 ? 16 : 32);
+    int total = 0;
+    for (int beta = 0; beta < 2; ++beta) {
+        for (int i = 0; i < 4 * bits; i += width) {
+            for (int ph = 0; ph < 32; ph += per_phase) {
+                int words_in_bank[32] = {};
+                uint32_t seen[32][32];
+                int nseen[32] = {};
+                int worst = 1;
+                for (int lane = ph; lane < ph + per_phase; ++lane) {
+                    const int gid = lane >> 2, t = lane & 3;
+                    const uint32_t a = (uint32_t)gid * stride + (uint32_t)(((128 * beta + 32 * t) * bits) >> 3) + i;
+                    for (uint32_t wd = a / 4; wd < (a + width) / 4; ++wd) {
+                        const int bank = (int)(wd % 32);
+                        bool dup = false;
+                        for (int k = 0; k < nseen[bank]; ++k) dup = dup || seen[bank][k] == wd;
+                        if (!dup && nseen[bank] < 32) {
+                            seen[bank][nseen[bank]++] = wd;
+                            words_in_bank[bank]++;
+                            worst = std::max(worst, words_in_bank[bank]);
+                        }
+                    }
+                }
+                total += worst;
+            }
+        }
+    }
+    return total;
+}
+
+std::atomic<uint32_t> g_pad_cache[8][8];   // [bits][(crow % 128) / 16]: pad + 1 (0 = unknown)
+std::atomic<int> g_sm_count[64];
+std::atomic<int> g_smem_set[64][64];   // [device][kernel variant]
+
+struct ClusterKey {
+    int dev, bits, ks, threads;
+    uint32_t smem;
+    bool operator<(const ClusterKey &o) const {
+        return std::tie(dev, bits, ks, threads, smem) < std::tie(o.dev, o.bits, o.ks, o.threads, o.smem);
+    }
+};
+std::mutex g_cluster_mu;
+std::map<ClusterKey, int> g_cluster_cache;
+
+}  // namespace
+
+uint32_t row_pad(int bits, uint32_t crow_bytes) {
+    const uint32_t key = (crow_bytes % 128u) / 16u;
+    std::atomic<uint32_t> &slot = g_pad_cache[bits & 7][key];
+    uint32_t v = slot.load(std::memory_order_relaxed);
+    if (v != 0) return v - 1;
+    uint32_t best = 16;
+    int best_w = 1 << 30;
+    for (uint32_t pad = 16; pad < 128; pad += 16) {
+        const int w = model_wavefronts(bits, crow_bytes + pad);
+        if (w < best_w) {
+            best_w = w;
+            best = pad;
+        }
+    }
+    slot.store(best + 1, std::memory_order_relaxed);
+    return best;
+}
+
+int sm_count_dev(int dev) {
+    if (dev < 0 || dev >= 64) return 0;
+    int v = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 0;
+    g_sm_count[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+bool set_smem_limit(const void *fn, int dev, int variant) {
+    if (dev < 0 || dev >= 64 || variant < 0 || variant >= 64) return false;
+    std::atomic<int> &slot = g_smem_set[dev][variant];
+    if (slot.load(std::memory_order_acquire) == 1) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    slot.store(1, std::memory_order_release);
+    return true;
+}
+
+int max_clusters(const void *fn, int dev, int ks, uint32_t smem, int variant, int threads) {
+    const ClusterKey key{dev, variant, ks, threads, smem};
+    {
+        std::lock_guard<std::mutex> lk(g_cluster_mu);
+        auto it = g_cluster_cache.find(key);
+        if (it != g_cluster_cache.end()) return it->second;
+    }
+    int n = 0;
+    if (ks == 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessorWithFlags(&per_sm, fn, threads, smem,
+                                                                   cudaOccupancyDefault) != cudaSuccess) {
+            cudaGetLastError();
+            per_sm = 0;
+        }
+        n = per_sm * sm_count_dev(dev);
+    } else {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(ks);
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = (unsigned)ks;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+    }
+    std::lock_guard<std::mutex> lk(g_cluster_mu);
+    g_cluster_cache[key] = n;
+    return n;
+}
+
+}  // namespace mma
+
+cudaError_t launch_qmv_mma(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
+                           const uint16_t *bias, uint16_t *y, int64_t M, int64_t K, int64_t N, int bits, int group,
+                           int64_t F, cudaStream_t stream) {
+    const int k = (int)K, n = (int)N, f = (int)F;
+    switch (bits) {
+        case 1: return mma::launch_b1(x, w, s, z, bias, y, M, k, n, group, f, stream);
+        case 2: return mma::launch_b2(x, w, s, z, bias, y, M, k, n, group, f, stream);
+        case 3: return mma::launch_b3(x, w, s, z, bias, y, M, k, n, group, f, stream);
+        case 4: return mma::launch_b4(x, w, s, z, bias, y, M, k, n, group, f, stream);
+        case 5: return mma::launch_b5(x, w, s, z, bias, y, M, k, n, group, f, stream);
+        case 6: return mma::launch_b6(x, w, s, z, bias, y, M, k, n, group, f, stream);
+        case 7: return mma::launch_b7(x, w, s, z, bias, y, M, k, n, group, f, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+uint32_t mma_timeouts(bool reset) {
+    return mma::timeouts_b1(reset) + mma::timeouts_b2(reset) + mma::timeouts_b3(reset) +
+           mma::timeouts_b4(reset) + mma::timeouts_b5(reset) + mma::timeouts_b6(reset) + mma::timeouts_b7(reset);
+}
+
+}  // namespace lowbit
