@@ -51,6 +51,9 @@
 // instead of hanging.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <atomic>
 #include <utility>
@@ -264,8 +267,10 @@ struct Params {
     uint32_t row_bytes;  // K * b / 8
     uint32_t crow_bytes; // Kc * b / 8 (one CTA's part of a row)
     uint32_t sstride;    // shared-memory bytes per staged row (padded)
-    uint32_t sz_off;     // within a stage: scales of its tiles (16 G fp16 per tile), then zeros
+    uint32_t sz_off;     // within a stage: scales of its tiles (16 x spg fp16 per tile), then zeros
     uint32_t z_off;
+    int spg;             // fp16 per staged row of scales / zeros (a padded box row)
+    int gcta;            // groups a CTA fetches from: rank * gcta (0: whole rows from group 0)
     uint32_t stage_bytes;
     uint32_t red_off, ring_off;
     uint32_t scr_off;    // per consumer warp: the B-fragment table of one row of x (kScrBytes)
@@ -314,22 +319,6 @@ __device__ __forceinline__ int64_t tile_row0(const Params &p, int lt) {
 __device__ __forceinline__ int tile_rows(const Params &p, int lt) {
     const int r0 = p.F == 0 ? lt * kTile : (lt >> 1) * kTile;
     return min(kTile, (p.F == 0 ? p.N : p.F) - r0);
-}
-
-// The unaligned ends of [ptr, ptr + bytes) are dropped: a hint never reaches
-// outside the range.
-__device__ __forceinline__ void prefetch_l2_inside(const void *ptr, uint64_t bytes) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
-    const uintptr_t b = (a + 15u) & ~(uintptr_t)15u;
-    const uintptr_t e = (a + bytes) & ~(uintptr_t)15u;
-    if (e > b) {
-        uint64_t n = e - b;
-        while (n > 0) {
-            const uint32_t c = (uint32_t)std::min<uint64_t>(n, 1u << 18);
-            ptx::bulk_prefetch_l2(reinterpret_cast<const void *>(b + (e - b - n)), c);
-            n -= c;
-        }
-    }
 }
 
 // 8 bf16 of x (16-byte aligned) as fp32.
@@ -388,7 +377,8 @@ __device__ __forceinline__ void red_arrive(bool cluster, uint32_t bar) {
 }
 
 template <int BITS, int MP, bool DB2>
-__global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 1)
+qmv_mma_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__ CUtensorMap zmap, const Params p) {
     static_assert(MP == 1 || MP == 2 || MP == 4 || MP == 8, "rows of x per column set");
     static_assert(!(DB2 && MP == 1), "one row of x always fits one column set");
     constexpr int NB = DB2 ? 2 : 1;                        // column sets per slice
@@ -420,28 +410,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const Params p) {
         }
         ptx::fence_mbar_init();
     }
-    if (warp == W && lane == 0 && rank == 0 && nst > 0) {
-        // Ask L2 for the first stages' weights while the previous kernel in the
-        // stream may still be running (a hint; L2 is coherent).
-        const int lt_end = lt0 + min(ntl, p.NS * p.RS);
-        if (p.F == 0) {
-            const int64_t r0 = tile_row0(p, lt0);
-            const int64_t r1 = tile_row0(p, lt_end - 1) + tile_rows(p, lt_end - 1);
-            prefetch_l2_inside(p.w + r0 * p.row_bytes, (uint64_t)(r1 - r0) * p.row_bytes);
-        } else {
-            for (int h = 0; h < 2; ++h) {
-                const int64_t r0 = tile_row0(p, lt0 + h);
-                const int64_t r1 = tile_row0(p, lt_end - 2 + h) + tile_rows(p, lt_end - 2 + h);
-                prefetch_l2_inside(p.w + r0 * p.row_bytes, (uint64_t)(r1 - r0) * p.row_bytes);
-            }
-        }
-    }
     if (clustered) ptx::cluster_sync();
     else __syncthreads();
-    ptx::pdl_wait();            // inputs may come from the previous kernel in the stream
 
     if (warp == W) {
-        // ---------------- producer: every lane issues row copies.
+        // ---------------- producer: every lane issues row copies.  It reads
+        // only packed weights, scales and zeros, which the previous kernel in
+        // the stream does not write (the library's interface requires it), so
+        // it starts at once: the first stages arrive while the consumers
+        // wait for that kernel and prepare x.
         const uint64_t pol = ptx::policy_evict_first();
         int s = 0;
         for (; s < nst; ++s) {
@@ -450,29 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const Params p) {
             const int lta = lt0 + s * p.RS;
             const int nts = min(p.RS, lt0 + ntl - lta);
             const uint32_t full = full0 + 8 * st;
-            uint8_t *stage = smem + p.ring_off + (size_t)st * p.stage_bytes;
             const uint32_t dst0 = sb + p.ring_off + (uint32_t)st * p.stage_bytes;
-            const uint32_t tsz = (uint32_t)(kTile * p.G * 2);          // bytes of one tile's scales
-            // A tile's scales (and zeros) are 16-byte aligned in global memory
-            // (the tile starts at a multiple of 16 rows); a ragged last tile may
-            // end inside a 16-byte chunk, whose bytes are copied with plain loads.
+            const uint32_t tsz = (uint32_t)(kTile * p.spg * 2);        // bytes of one tile's scales
+            // Scales and zeros: one 2D tensor copy each per tile, a box of 16
+            // rows x spg fp16 from group rank * gcta (rows past the matrix and
+            // columns past its groups read as zero).
             uint32_t bytes = 0;
-            for (int i = 0; i < nts; ++i) {
-                const int nr = tile_rows(p, lta + i);
-                const uint32_t b = (uint32_t)nr * (uint32_t)p.G * 2u;
-                bytes += (uint32_t)nr * p.crow_bytes + 2u * (b & ~15u);
-                if (b & 15u) {
-                    const int64_t e0 = tile_row0(p, lta + i) * p.G + (b & ~15u) / 2;
-                    const int n = (int)((b & 15u) / 2);
-                    uint16_t *ds = reinterpret_cast<uint16_t *>(stage + p.sz_off + i * tsz + (b & ~15u));
-                    uint16_t *dz = reinterpret_cast<uint16_t *>(stage + p.z_off + i * tsz + (b & ~15u));
-                    if (lane < n) {
-                        ds[lane] = p.s[e0 + lane];
-                        dz[lane] = p.z[e0 + lane];
-                    }
-                }
-            }
-            __syncwarp();
+            for (int i = 0; i < nts; ++i) bytes += (uint32_t)tile_rows(p, lta + i) * p.crow_bytes + 2u * tsz;
             if (lane == 0) ptx::mbar_arrive_expect_tx(full, bytes);
             __syncwarp();
             for (int i = 0; i < nts; ++i) {
@@ -482,10 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const Params p) {
                 for (int r = lane; r < nr; r += 32)
                     ptx::bulk_g2s(dst0 + (uint32_t)(i * kTile + r) * p.sstride, src + (int64_t)r * p.row_bytes,
                                   p.crow_bytes, full, pol);
-                const uint32_t b = ((uint32_t)nr * (uint32_t)p.G * 2u) & ~15u;
-                if (lane == 31 && b > 0) {
-                    ptx::bulk_g2s(dst0 + p.sz_off + i * tsz, p.s + g0 * p.G, b, full, pol);
-                    ptx::bulk_g2s(dst0 + p.z_off + i * tsz, p.z + g0 * p.G, b, full, pol);
+                if (lane == 31) {
+                    ptx::tma_load_2d_hint(dst0 + p.sz_off + i * tsz, &smap, rank * p.gcta, (int)g0, full, pol);
+                    ptx::tma_load_2d_hint(dst0 + p.z_off + i * tsz, &zmap, rank * p.gcta, (int)g0, full, pol);
                 }
             }
         }
@@ -494,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const Params p) {
             if (!ptx::mbar_wait(full0 + 8 * (i % p.NS), (i / p.NS) & 1, &g_mma_timeouts)) break;
     } else if (warp == W + 1) {
         // ---------------- finisher (first CTA of the cluster): sum the partials.
+        ptx::pdl_wait();            // y and bias: only after the previous kernel in the stream
         if (rank == 0) {
             const int nsrc = ks * W;
             const int rows_stage = p.RS * kTile;
@@ -544,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const Params p) {
         }
     } else {
         // ---------------- consumers.
+        ptx::pdl_wait();            // x may come from the previous kernel in the stream
         const int gid = lane >> 2, t = lane & 3;
         const int M = p.M;
         const int kw0 = rank * p.Kc + warp * kSlice;          // first code of this warp's slice
@@ -575,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const Params p) {
         // MP == 1: columns 2t, 2t + 1 are adjacent groups (both used or both
         // unused when the slice has two or more groups), read as one word.
         const bool pair_sz = MP == 1 && gsl >= 2;
-        const int gpair = gw0 + ((MP == 1 && 2 * t < gsl) ? 2 * t : 0);
+        const int gbase = rank * p.gcta;                      // first group of a staged scale row
+        const int gpair = gw0 - gbase + ((MP == 1 && 2 * t < gsl) ? 2 * t : 0);
 
         // Per x row: the scale 2^e, and the group sums X and O of this thread's columns.
         // Per x row m: the scale 2^e of the warp's slice, the group sums X and O
@@ -687,12 +650,12 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const Params p) {
             const int redi0 = buf * (int)p.red_floats + src * rows_stage * MP;
             for (int i = 0; i < nts && ok; ++i) {
                 // Scales and zeros of rows gid, gid + 8 (read before the MMAs).
-                const uint16_t *ts = reinterpret_cast<const uint16_t *>(stage + p.sz_off) + i * kTile * p.G;
-                const uint16_t *tz = reinterpret_cast<const uint16_t *>(stage + p.z_off) + i * kTile * p.G;
+                const uint16_t *ts = reinterpret_cast<const uint16_t *>(stage + p.sz_off) + i * kTile * p.spg;
+                const uint16_t *tz = reinterpret_cast<const uint16_t *>(stage + p.z_off) + i * kTile * p.spg;
                 float sv[2][NB][2], zv[2][NB][2];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const int ro = (gid + 8 * r) * p.G;
+                    const int ro = (gid + 8 * r) * p.spg;
                     if (pair_sz) {
                         const uint32_t s2 = *reinterpret_cast<const uint32_t *>(ts + ro + gpair);
                         const uint32_t z2 = *reinterpret_cast<const uint32_t *>(tz + ro + gpair);
@@ -707,8 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const Params p) {
                                     sv[r][bb][1] = sv[r][bb][0];
                                     zv[r][bb][1] = zv[r][bb][0];
                                 } else {
-                                    sv[r][bb][e] = half_bits_to_float(ts[ro + gk[bb][e]]);
-                                    zv[r][bb][e] = half_bits_to_float(tz[ro + gk[bb][e]]);
+                                    sv[r][bb][e] = half_bits_to_float(ts[ro + gk[bb][e] - gbase]);
+                                    zv[r][bb][e] = half_bits_to_float(tz[ro + gk[bb][e] - gbase]);
                                 }
                             }
                     }
@@ -789,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const Params p) {
 struct LaunchPlan {
     bool ok = false;
     Params prm{};
+    CUtensorMap smap, zmap;
     int grid = 0;
     int threads = 0;
     uint32_t smem = 0;
@@ -801,6 +765,11 @@ inline int max_rows(int group) { return group == 32 ? 2 : (group == 64 ? 4 : 8);
 // conflicts for the consumers' reads (row gid of lane 4 gid + t reads its two
 // blocks at slice bytes (128 beta + 32 t) b / 8).
 uint32_t row_pad(int bits, uint32_t crow_bytes);
+// Padded length (fp16) of a staged row of `groups` scales, from a model of the
+// epilogue's reads (see qmv_mma_host.cu), and 2D tensor-map encoding.
+int sz_pitch(int groups, int gsl, int MP, int W);
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, uint64_t inner, uint64_t rows,
+               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
 
 int sm_count_dev(int dev);
 // Clusters of ks CTAs (smem bytes each, kThreads threads) that fit at once, per device.
@@ -856,10 +825,18 @@ LaunchPlan plan_launch(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
     q.row_bytes = (uint32_t)((int64_t)K * BITS / 8);
     q.crow_bytes = (uint32_t)((int64_t)q.Kc * BITS / 8);
     q.sstride = q.crow_bytes + row_pad(BITS, q.crow_bytes);
+    // Scales and zeros: a CTA fetches its own groups when they start on a
+    // 16-byte boundary, else whole rows; the box row is padded (over-read)
+    // so that the epilogue's reads of 16 rows fall into distinct banks.
+    if ((q.G * 2) % 16 != 0) return pl;                     // rows of scales must be 16-byte multiples
+    const int gc = q.Kc / group;
+    q.gcta = (ks == 1 || (gc * 2) % 16 == 0) ? gc : 0;
+    q.spg = sz_pitch(q.gcta != 0 ? gc : q.G, std::max(1, kSlice / group), q.MP, q.W);
+    if (q.spg > 256) return pl;
     constexpr uint32_t kBudget = 227u * 1024u;
     constexpr uint32_t kBars = 16u * kMaxStages + 16u * kRedBufs;
     for (int rs = 8; rs >= q.unit; rs -= q.unit) {
-        const uint32_t stage = (uint32_t)rs * kTile * (q.sstride + 4u * (uint32_t)q.G);
+        const uint32_t stage = (uint32_t)rs * kTile * (q.sstride + 4u * (uint32_t)q.spg);
         if (rs > q.unit && stage > 72u * 1024u) continue;
         const uint32_t red_floats = (uint32_t)(ks * q.W * rs * kTile * q.MP);
         const uint32_t red_off = (kBars + 127u) & ~127u;
@@ -872,7 +849,7 @@ LaunchPlan plan_launch(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
         q.NS = ns;
         q.stage_bytes = stage;
         q.sz_off = (uint32_t)rs * kTile * q.sstride;
-        q.z_off = q.sz_off + (uint32_t)rs * kTile * (uint32_t)q.G * 2u;
+        q.z_off = q.sz_off + (uint32_t)rs * kTile * (uint32_t)q.spg * 2u;
         q.red_floats = red_floats;
         q.red_off = red_off;
         q.scr_off = scr_off;
@@ -881,6 +858,12 @@ LaunchPlan plan_launch(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
         break;
     }
     if (q.RS == 0) return pl;
+    const int rows_total = F != 0 ? 2 * F : N;
+    if (!encode_2d(&pl.smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, s, (uint64_t)q.G, (uint64_t)rows_total,
+                   (uint64_t)q.G * 2, (uint32_t)q.spg, kTile) ||
+        !encode_2d(&pl.zmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, z, (uint64_t)q.G, (uint64_t)rows_total,
+                   (uint64_t)q.G * 2, (uint32_t)q.spg, kTile))
+        return pl;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return pl;
     const void *fn = kernel_ptr<BITS>(q.MP, q.DB == 2);
@@ -914,10 +897,10 @@ cudaError_t launch_plan(const LaunchPlan &pl, cudaStream_t stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pl.prm.ks > 1 ? 2 : 1;
-    using KFn = void (*)(const Params);
+    using KFn = void (*)(const CUtensorMap, const CUtensorMap, const Params);
     const KFn fn = reinterpret_cast<KFn>(const_cast<void *>(kernel_ptr<BITS>(pl.prm.MP, pl.prm.DB == 2)));
     if (fn == nullptr) return cudaErrorInvalidValue;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, pl.prm);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, pl.smap, pl.zmap, pl.prm);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

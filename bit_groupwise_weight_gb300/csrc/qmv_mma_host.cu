@@ -60,6 +60,65 @@ int model_wavefronts(int bits, uint32_t stride) {
     return total;
 }
 
+// Wavefronts of one warp-wide shared load: `addr` per lane, `width` bytes
+// each (phases of 32, 16 or 8 lanes for 4-, 8- and 16-byte loads).
+int warp_wavefronts(const uint32_t (&addr)[32], int width) {
+    const int per_phase = width == 16 ? 8 : (width == 8 ? 16 : 32);
+    int total = 0;
+    for (int ph = 0; ph < 32; ph += per_phase) {
+        uint32_t words[32][8];
+        int n[32] = {};
+        int worst = 1;
+        for (int l = ph; l < ph + per_phase; ++l)
+            for (uint32_t wd = addr[l] / 4; wd < (addr[l] + (uint32_t)std::max(width, 4)) / 4; ++wd) {
+                const int bank = (int)(wd % 32);
+                bool dup = false;
+                for (int k = 0; k < n[bank]; ++k) dup = dup || words[bank][k] == wd;
+                if (!dup && n[bank] < 8) {
+                    words[bank][n[bank]++] = wd;
+                    worst = std::max(worst, n[bank]);
+                }
+            }
+        total += worst;
+    }
+    return total;
+}
+
+// The epilogue's scale reads for a staged row of spg fp16: lane 4 gid + t
+// of warp w reads row gid at group w * gsl + c, c = 2t as a 32-bit pair (one
+// row of x, two or more groups per slice) or (2t) / MP as 16 bits.
+int sz_model(int spg, int gsl, int MP, int W) {
+    int total = 0;
+    const bool pair = MP == 1 && gsl >= 2;
+    for (int w = 0; w < W; ++w) {
+        uint32_t a[32];
+        for (int l = 0; l < 32; ++l) {
+            const int gid = l >> 2, t = l & 3;
+            const int c = pair ? ((2 * t < gsl) ? 2 * t : 0) : std::min((2 * t) / MP, gsl - 1);
+            a[l] = (uint32_t)((gid * spg + w * gsl + c) * 2);
+        }
+        total += warp_wavefronts(a, pair ? 4 : 2);
+    }
+    return total;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_entry() {
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load(std::memory_order_acquire);
+    if (f == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f, std::memory_order_release);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+std::mutex g_spg_mu;
+std::map<std::tuple<int, int, int, int>, int> g_spg_cache;
+
 std::atomic<uint32_t> g_pad_cache[8][8];   // [bits][(crow % 128) / 16]: pad + 1 (0 = unknown)
 std::atomic<int> g_sm_count[64];
 std::atomic<int> g_smem_set[64][64];   // [device][kernel variant]
@@ -92,6 +151,40 @@ uint32_t row_pad(int bits, uint32_t crow_bytes) {
     }
     slot.store(best + 1, std::memory_order_relaxed);
     return best;
+}
+
+int sz_pitch(int groups, int gsl, int MP, int W) {
+    const auto key = std::make_tuple(groups, gsl, MP, W);
+    {
+        std::lock_guard<std::mutex> lk(g_spg_mu);
+        auto it = g_spg_cache.find(key);
+        if (it != g_spg_cache.end()) return it->second;
+    }
+    const int base = std::max(8, (groups + 7) & ~7);
+    int best = base, best_w = 1 << 30;
+    for (int spg = base; spg <= base + 32; spg += 8) {
+        const int wf = sz_model(spg, gsl, MP, W);
+        if (wf < best_w) {
+            best_w = wf;
+            best = spg;
+        }
+    }
+    std::lock_guard<std::mutex> lk(g_spg_mu);
+    g_spg_cache[key] = best;
+    return best;
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, uint64_t inner, uint64_t rows,
+               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_entry();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, type, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int sm_count_dev(int dev) {
