@@ -28,6 +28,18 @@
  *     caller's next synchronisation, as for any CUDA kernel.
  *   - Arguments are checked on the host before anything is launched; a call
  *     that returns anything but LOWBIT_OK has launched nothing.
+ *   - Overlap with the previous kernel in the stream: the linear entry points
+ *     launch with programmatic dependent launch, and the decode kernel starts
+ *     reading the packed weights, scales and zeros before the previous kernel
+ *     in the stream has finished, when that kernel allows it (this library's
+ *     linear kernels do, as soon as they start).  x and bias are read, and y
+ *     written, only after the previous kernel has completed.  So the packed
+ *     weights, scales and zeros of a linear call must not be written by the
+ *     kernel immediately before it in the stream if that kernel is one of
+ *     this library's linear kernels (which write only y) or another kernel
+ *     that allows early launch.  Ordinary kernels and copies, and this
+ *     library's packing and quantising kernels, do not allow it: weights they
+ *     produce are always seen complete.
  *   - 16-bit floats are passed as their bit patterns (uint16_t): bf16 for x and
  *     y, IEEE binary16 (fp16) for scales, zeros and bias.
  *   - The library holds no global handle; calls from several host threads are
