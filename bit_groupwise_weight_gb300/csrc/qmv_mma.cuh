@@ -293,22 +293,21 @@ uint32_t read_timeouts(bool reset) {
 }
 }  // namespace
 
-// The b words of a 32-code block from shared memory, with the widest loads
-// its alignment allows (block offsets are multiples of 4 b bytes).
-template <int BITS>
-__device__ __forceinline__ void lds_block_bits(const uint8_t *p, uint32_t (&w)[BITS]) {
+// The b words of a 32-code block from shared memory (byte address + OFF),
+// with the widest loads its alignment allows (block offsets are multiples of
+// 4 b bytes).
+template <int BITS, int OFF>
+__device__ __forceinline__ void lds_block_bits(uint32_t addr, uint32_t (&w)[BITS]) {
     if constexpr (BITS == 4) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(p);
-        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        ptx::lds_v4<OFF>(addr, w[0], w[1], w[2], w[3]);
     } else if constexpr (BITS == 2 || BITS == 6) {
-#pragma unroll
-        for (int i = 0; i < BITS / 2; ++i) {
-            const uint2 v = *reinterpret_cast<const uint2 *>(p + 8 * i);
-            w[2 * i] = v.x; w[2 * i + 1] = v.y;
-        }
+        [&]<int... I>(std::integer_sequence<int, I...>) {
+            (ptx::lds_v2<OFF + 8 * I>(addr, w[2 * I], w[2 * I + 1]), ...);
+        }(std::make_integer_sequence<int, BITS / 2>{});
     } else {
-#pragma unroll
-        for (int i = 0; i < BITS; ++i) w[i] = reinterpret_cast<const uint32_t *>(p)[i];
+        [&]<int... I>(std::integer_sequence<int, I...>) {
+            ((w[I] = ptx::lds_u32_off<OFF + 4 * I>(addr)), ...);
+        }(std::make_integer_sequence<int, BITS>{});
     }
 }
 
@@ -349,11 +348,11 @@ __device__ __forceinline__ float hi_half(uint32_t v) { return half_bits_to_float
 // between two accumulators (shorter dependency chains); with two, block BETA
 // accumulates into its own.
 template <int BITS, bool DB2, int BETA>
-__device__ __forceinline__ void tile_block(const uint8_t *rowa, const uint8_t *rowb, int boff,
-                                           const uint32_t (&bq)[16][2], float (&d0)[4], float (&d1)[4]) {
+__device__ __forceinline__ void tile_block(uint32_t rowa, uint32_t rowb, const uint32_t (&bq)[16][2],
+                                           float (&d0)[4], float (&d1)[4]) {
     uint32_t wa[BITS], wb[BITS];
-    lds_block_bits<BITS>(rowa + boff, wa);
-    lds_block_bits<BITS>(rowb + boff, wb);
+    lds_block_bits<BITS, BETA * 16 * BITS>(rowa, wa);
+    lds_block_bits<BITS, BETA * 16 * BITS>(rowb, wb);
     [&]<int... C>(std::integer_sequence<int, C...>) {
         ((void)[&] {
             const uint32_t a0 = code_pair<BITS, 2 * C>(wa), a1 = code_pair<BITS, 2 * C>(wb);
@@ -629,36 +628,50 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__
             }
         }
 
-        // This warp's part of a staged row, and the reduction buffer of the
-        // cluster's first CTA (this CTA's own when there is no cluster).
-        const uint32_t wslice = (uint32_t)warp * (kSlice * BITS / 8);
-        const uint32_t red_remote = clustered ? ptx::mapa_shared(sb + p.red_off, 0u) : sb + p.red_off;
+        // Shared-memory byte offsets, fixed per thread: row gid's first block
+        // within a staged tile, row gid + 8 from there, a tile's stride; the
+        // scales of rows gid and gid + 8 within a tile's scale box (the zeros
+        // sit zdelta bytes after their scales); this thread's slot in a
+        // reduction buffer of the cluster's first CTA (this CTA's own when
+        // there is no cluster).
+        const uint32_t a_off = (uint32_t)gid * p.sstride + (uint32_t)warp * (kSlice * BITS / 8) +
+                               (uint32_t)((32 * t * BITS) >> 3);
+        const uint32_t b_off = 8u * p.sstride;
+        const uint32_t t_str = (uint32_t)kTile * p.sstride;
+        const uint32_t tsz = (uint32_t)(kTile * p.spg * 2);
+        const uint32_t zdelta = p.z_off - p.sz_off;
+        const uint32_t r8 = (uint32_t)(16 * p.spg);                      // 8 scale rows, bytes
+        const uint32_t srow0 = (uint32_t)(2 * gid * p.spg);
+        uint32_t so[NB][2];
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) so[bb][e] = srow0 + 2u * (uint32_t)(gk[bb][e] - gbase);
+        const uint32_t so_pair = srow0 + 2u * (uint32_t)gpair;
+        const uint32_t red_base = (clustered ? ptx::mapa_shared(sb + p.red_off, 0u) : sb + p.red_off) +
+                                  4u * (uint32_t)((rank * W + warp) * p.RS * kTile * MP);
+        const uint32_t red_buf_bytes = 4u * p.red_floats;
         const uint32_t rfull_leader = clustered ? ptx::mapa_shared(rfull0, 0u) : rfull0;
-        float *red_local = reinterpret_cast<float *>(smem + p.red_off);
-        const int src = rank * W + warp;
-        const int rows_stage = p.RS * kTile;
-        const int boff0 = (32 * t * BITS) >> 3, boff1 = ((128 + 32 * t) * BITS) >> 3;
 
         bool ok = true;
+        uint32_t stage = sb + p.ring_off, fpar = 0;       // ring stage of step s, its index and parity
+        int st = 0;
         for (int s = 0; s < nst; ++s) {
-            const int st = s % p.NS, buf = s % kRedBufs;
-            if (ok) ok = ptx::mbar_wait(full0 + 8 * st, (s / p.NS) & 1, &g_mma_timeouts);
+            const int buf = s % kRedBufs;
+            if (ok) ok = ptx::mbar_wait(full0 + 8 * st, fpar, &g_mma_timeouts);
             if (ok && s >= kRedBufs) ok = red_wait(clustered, rfree0 + 8 * buf, ((s / kRedBufs) - 1) & 1);
-            const int lta = lt0 + s * p.RS;
-            const int nts = min(p.RS, lt0 + ntl - lta);
-            const uint8_t *stage = smem + p.ring_off + (size_t)st * p.stage_bytes;
-            const int redi0 = buf * (int)p.red_floats + src * rows_stage * MP;
-            for (int i = 0; i < nts && ok; ++i) {
+            const int nts = min(p.RS, ntl - s * p.RS);
+            uint32_t tile = stage + a_off, sz = stage + p.sz_off;
+            uint32_t red = red_base + (uint32_t)buf * red_buf_bytes;
+            for (int i = 0; i < nts && ok; ++i, tile += t_str, sz += tsz, red += 4u * kTile * MP) {
                 // Scales and zeros of rows gid, gid + 8 (read before the MMAs).
-                const uint16_t *ts = reinterpret_cast<const uint16_t *>(stage + p.sz_off) + i * kTile * p.spg;
-                const uint16_t *tz = reinterpret_cast<const uint16_t *>(stage + p.z_off) + i * kTile * p.spg;
                 float sv[2][NB][2], zv[2][NB][2];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const int ro = (gid + 8 * r) * p.spg;
+                    const uint32_t rs = sz + (r ? r8 : 0u);
                     if (pair_sz) {
-                        const uint32_t s2 = *reinterpret_cast<const uint32_t *>(ts + ro + gpair);
-                        const uint32_t z2 = *reinterpret_cast<const uint32_t *>(tz + ro + gpair);
+                        const uint32_t s2 = ptx::lds_u32(rs + so_pair);
+                        const uint32_t z2 = ptx::lds_u32(rs + so_pair + zdelta);
                         sv[r][0][0] = lo_half(s2); sv[r][0][1] = hi_half(s2);
                         zv[r][0][0] = lo_half(z2); zv[r][0][1] = hi_half(z2);
                     } else {
@@ -670,17 +683,15 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__
                                     sv[r][bb][1] = sv[r][bb][0];
                                     zv[r][bb][1] = zv[r][bb][0];
                                 } else {
-                                    sv[r][bb][e] = half_bits_to_float(ts[ro + gk[bb][e] - gbase]);
-                                    zv[r][bb][e] = half_bits_to_float(tz[ro + gk[bb][e] - gbase]);
+                                    sv[r][bb][e] = half_bits_to_float(ptx::lds_u16(rs + so[bb][e]));
+                                    zv[r][bb][e] = half_bits_to_float(ptx::lds_u16(rs + so[bb][e] + zdelta));
                                 }
                             }
                     }
                 }
-                const uint8_t *rowa = stage + (size_t)(i * kTile + gid) * p.sstride + wslice;
-                const uint8_t *rowb = rowa + 8 * p.sstride;
                 float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-                tile_block<BITS, DB2, 0>(rowa, rowb, boff0, bq, d0, d1);
-                tile_block<BITS, DB2, 1>(rowa, rowb, boff1, bq, d0, d1);
+                tile_block<BITS, DB2, 0>(tile, tile + b_off, bq, d0, d1);
+                tile_block<BITS, DB2, 1>(tile, tile + b_off, bq, d0, d1);
                 float acc[2][2];
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
@@ -697,11 +708,10 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__
                     }
                 // Sum over the lanes that hold the same (row, x row), then store
                 // this warp's partial sums, in units of x (times 2^-e).
-                const int ri = redi0 + i * kTile * MP;
                 auto put = [&](int row, int m, float v) {
-                    const int idx = ri + row * MP + m;
-                    if (clustered) ptx::st_cluster_f32(red_remote + (uint32_t)idx * 4u, v);
-                    else red_local[idx] = v;
+                    const uint32_t a = red + 4u * (uint32_t)(row * MP + m);
+                    if (clustered) ptx::st_cluster_f32(a, v);
+                    else ptx::sts_f32(a, v);
                 };
                 if constexpr (MP == 1) {
                     float v0 = acc[0][0] + acc[0][1], v1 = acc[1][0] + acc[1][1];
@@ -740,6 +750,12 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__
             if (lane == 0) {
                 ptx::mbar_arrive(empty0 + 8 * st);
                 red_arrive(clustered, rfull_leader + 8 * buf);
+            }
+            stage += p.stage_bytes;
+            if (++st == p.NS) {
+                st = 0;
+                stage = sb + p.ring_off;
+                fpar ^= 1u;
             }
         }
     }
