@@ -55,11 +55,8 @@ def _bind(lib):
 
 
 def library_path() -> Path:
-    """The in-tree build, or the file named by $LOWBIT_LIBRARY (another build of
-    the same sources, e.g. with different compile-time tuning)."""
-    import os
-    override = os.environ.get("LOWBIT_LIBRARY")
-    return Path(override) if override else _build.LIB
+    """The in-tree build of the library (the only one this binding loads)."""
+    return _build.LIB
 
 
 def abi():

@@ -88,15 +88,20 @@ lowbit_status check_linear_args(const uint16_t *x, const uint8_t *w, const uint1
     return LOWBIT_OK;
 }
 
-// Crossover between the CUDA-core kernel (reads the weights once per two rows
-// of x) and the tensor-core kernel (time nearly independent of M up to 32),
-// measured on GB300 for the Llama-3.1-8B shapes at b = 4, g = 128.  The
-// tensor-core kernel splits K over a cluster when its row tiles are too few to
-// fill the GPU (N below ~9400 outputs); then it wins from M = 3 or 5, while
-// for wider layers the CUDA-core kernel stays ahead up to M = 6.
+// Crossover between the decode kernels and the batched tensor-core kernel
+// (qmm), measured on GB300 for the Llama-3.1-8B shapes at b = 4, g = 128,
+// M = 2..32.  The tensor-core decode kernel reads the weights once per launch
+// of up to 2 (g = 32), 4 (g = 64) or 8 (g >= 128) rows of x; qmm's time is
+// nearly flat in M up to 32.  One decode launch beat qmm on every shape (down
+// at M = 8: 31.7 vs 32.8 us); two launches beat it only for the widest layer
+// (gate+up, N = 28672: 50 vs 66 us at M = 16; qkv, o and down lost).  Where
+// the decode kernel does not take the shape, the CUDA-core kernel reads the
+// weights once per two rows of x and wins up to M = 2, or up to M = 6 for
+// layers of N >= 9424 outputs.
 constexpr int64_t kQmvMaxM = 2;
 constexpr int64_t kQmvMaxMWide = 6;
 constexpr int64_t kWideN = 9424;          // 76 row tiles of 124: half the SMs
+constexpr int64_t kTwoPassN = 20000;      // two decode launches still beat qmm
 
 }  // namespace
 
@@ -157,9 +162,14 @@ lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int gr
     if (!bits_ok(bits) || !group_ok(group) || M < 0 || N < 0 || K <= 0 || K % group != 0 ||
         M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return LOWBIT_PATH_AUTO;
-    // The tensor-core kernel needs K % 128 == 0; other shapes stay on the CUDA-core kernel.
-    if (K % 128 != 0 || M <= kQmvMaxM || (M <= kQmvMaxMWide && N >= kWideN)) return LOWBIT_PATH_QMV;
-    return LOWBIT_PATH_QMM;
+    // qmm needs K % 128 == 0; other shapes stay on the decode kernels.
+    if (K % 128 != 0) return LOWBIT_PATH_QMV;
+    if (lowbit::qmv_mma_shape_ok(K, group)) {
+        const int64_t rows = lowbit::qmv_mma_rows(group);
+        const int64_t passes = (M + rows - 1) / rows;
+        return (passes <= 1 || (passes == 2 && N >= kTwoPassN)) ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
+    }
+    return (M <= kQmvMaxM || (M <= kQmvMaxMWide && N >= kWideN)) ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
 }
 
 lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *packed_w, const uint16_t *scales,

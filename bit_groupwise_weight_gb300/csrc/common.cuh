@@ -142,6 +142,17 @@ cudaError_t launch_quantize(const void *w, int dtype, uint8_t *packed, uint16_t 
 cudaError_t launch_qmv_mma(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
                            const uint16_t *bias, uint16_t *y, int64_t M, int64_t K, int64_t N, int bits, int group,
                            int64_t F, cudaStream_t stream);
+// Per-device host state (device.cu), keyed by device ordinal and kernel; a
+// failed query returns 0 (or its error) and is not cached.
+int current_device();                                                   // -1 on error
+int device_sm_count(int dev);
+cudaError_t raise_smem_limit(const void *fn, int dev, int bytes);       // once per (device, kernel, bytes)
+int blocks_per_sm(const void *fn, int dev, int threads, uint32_t smem);
+int clusters_at_once(const void *fn, int dev, int ks, int threads, uint32_t smem);
+// True when the tensor-core decode kernel takes K and group (given 16-byte
+// aligned x, weights, scales and zeros), and the rows of x it takes per launch.
+bool qmv_mma_shape_ok(int64_t K, int group);
+int qmv_mma_rows(int group);
 // Bounded waits that gave up, per kernel file (device counters; reading syncs).
 uint32_t mma_timeouts(bool reset);
 uint32_t qmv_timeouts(bool reset);

@@ -509,51 +509,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
 }
 
-std::atomic<int> g_smem_attr_set[8];
-
-int device_sm_count() {
-    static std::atomic<int> cached{0};
-    int v = cached.load(std::memory_order_relaxed);
-    if (v > 0) return v;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-    cached.store(sms, std::memory_order_relaxed);
-    return sms;
-}
-
-// Whether `clusters` clusters of ks CTAs (smem bytes each) can all be resident
-// at once.  Cached per (bit width, ks) for the last shared-memory size asked.
-template <int BITS>
-bool cluster_fits(int ks, uint32_t smem, int clusters) {
-    static std::atomic<uint64_t> cache[9];                // (smem << 32) | (max clusters + 1)
-    uint64_t c = cache[ks].load(std::memory_order_relaxed);
-    int maxc;
-    if (c != 0 && (uint32_t)(c >> 32) == smem) {
-        maxc = (int)(uint32_t)c - 1;
-    } else {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(ks * clusters);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = smem;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = (unsigned)ks;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        maxc = 0;
-        if (cudaOccupancyMaxActiveClusters(&maxc, qmm_kernel<BITS>, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            maxc = 0;
-        }
-        cache[ks].store(((uint64_t)smem << 32) | (uint32_t)(maxc + 1), std::memory_order_relaxed);
-    }
-    return maxc >= clusters;
-}
-
 template <int BITS>
 cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
                         const uint16_t *bias, uint16_t *y, int M, int K, int N, int group,
@@ -606,11 +561,11 @@ cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, 
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    if (g_smem_attr_set[BITS].load(std::memory_order_relaxed) == 0) {
-        cudaFuncSetAttribute(reinterpret_cast<const void *>(&qmm_kernel<BITS>),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        g_smem_attr_set[BITS].store(1, std::memory_order_relaxed);
-    }
+    const void *kfn = reinterpret_cast<const void *>(&qmm_kernel<BITS>);
+    const int dev = current_device();
+    const int sms = dev < 0 ? 0 : device_sm_count(dev);
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    if (const cudaError_t e = raise_smem_limit(kfn, dev, 227 * 1024); e != cudaSuccess) return e;
     // Split K over a cluster when the row and batch tiles alone leave SMs idle:
     // as many CTAs per tile as fill the SMs (at most 8, whole groups each),
     // provided every cluster can be resident at once and the partial sums fit
@@ -621,10 +576,10 @@ cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, 
     const int units = q.ktiles / q.kt_unit;
     q.recv_off = q.x_off;
     int ks = 1;
-    if (tiles < device_sm_count()) ks = std::min(std::min(8, device_sm_count() / tiles), units);
+    if (tiles < sms) ks = std::min(std::min(8, sms / tiles), units);
     while (ks > 1) {
         const uint32_t need = (uint32_t)(ks * ((4 + ks - 1) / ks)) * 256u * 64u;
-        if (q.recv_off + need <= smem - 1024u && cluster_fits<BITS>(ks, smem, tiles)) break;
+        if (q.recv_off + need <= smem - 1024u && clusters_at_once(kfn, dev, ks, kThreads, smem) >= tiles) break;
         --ks;
     }
     q.ksplit = ks;

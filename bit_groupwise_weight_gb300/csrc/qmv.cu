@@ -683,40 +683,14 @@ const void *stream_kernel_ptr() {
     return reinterpret_cast<const void *>(&qmv_stream_kernel<BITS, M, LUT>);
 }
 
-// Resident CTAs per SM for (bits, M, warps, shared-memory bucket of 8 KB),
-// cached; 0 = not yet known.  The bucket's upper edge is used, so the value is
-// never optimistic.  Also sets the kernel's dynamic shared-memory limit on
-// first use.
-std::atomic<int> g_occ_cache[8][3][18][26];
-
+// Resident CTAs per SM of the stream kernel on device dev, for a shared-memory
+// size rounded up to the next 8 KB (never optimistic; few distinct queries),
+// with the kernel's dynamic shared-memory limit raised first.  0 on error.
 template <int BITS, int M, bool LUT>
-int stream_occupancy(int threads, uint32_t smem) {
-    const int ti = threads / 32;
-    const int si = (int)((smem + 8191u) / 8192u);
-    if (ti >= 18 || si >= 26) return 1;
-    std::atomic<int> &slot = g_occ_cache[LUT ? 0 : BITS][M][ti][si];   // slot 0: the table-decode kernel
-    int v = slot.load(std::memory_order_relaxed);
-    if (v > 0) return v;
+int stream_occupancy(int dev, int threads, uint32_t smem) {
     const void *fn = stream_kernel_ptr<BITS, M, LUT>();
-    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, (size_t)si * 8192u) != cudaSuccess ||
-        occ < 1)
-        occ = 1;
-    slot.store(occ, std::memory_order_relaxed);
-    return occ;
-}
-
-int sm_count() {
-    static std::atomic<int> cached{0};
-    int v = cached.load(std::memory_order_relaxed);
-    if (v > 0) return v;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-    cached.store(sms, std::memory_order_relaxed);
-    return sms;
+    if (raise_smem_limit(fn, dev, 200 * 1024) != cudaSuccess) return 0;
+    return blocks_per_sm(fn, dev, threads, (smem + 8191u) / 8192u * 8192u);
 }
 
 // Shared memory a CTA may fill with ring stages (two CTAs fit on an SM).
@@ -769,8 +743,11 @@ StreamPlan plan_stream(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
     pl.threads = q.T + 32;
     q.total_passes = F != 0 ? 2 * ((F + q.R - 1) / q.R) : (N + q.R - 1) / q.R;
     q.chunks = (q.total_passes + q.chunk - 1) / q.chunk;
-    const int occ = stream_occupancy<BITS, M, LUT>(pl.threads, pl.smem);
-    pl.grid = std::max(1, std::min(q.chunks, sm_count() * occ));
+    const int dev = current_device();
+    const int occ = dev < 0 ? 0 : stream_occupancy<BITS, M, LUT>(dev, pl.threads, pl.smem);
+    const int sms = dev < 0 ? 0 : device_sm_count(dev);
+    if (occ < 1 || sms < 1) return pl;                 // pl.ok stays false: a CUDA error
+    pl.grid = std::max(1, std::min(q.chunks, sms * occ));
     q.chunks_base = q.chunks / pl.grid;
     q.chunks_extra = q.chunks % pl.grid;
     pl.ok = true;

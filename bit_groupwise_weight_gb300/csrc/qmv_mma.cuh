@@ -787,10 +787,8 @@ int sz_pitch(int groups, int gsl, int MP, int W);
 bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, uint64_t inner, uint64_t rows,
                uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
 
-int sm_count_dev(int dev);
-// Clusters of ks CTAs (smem bytes each, kThreads threads) that fit at once, per device.
-int max_clusters(const void *fn, int dev, int ks, uint32_t smem, int variant, int threads);
-bool set_smem_limit(const void *fn, int dev, int variant);
+// Clusters of ks CTAs (smem bytes, `threads` threads each) resident at once on device dev.
+int max_clusters(const void *fn, int dev, int ks, uint32_t smem, int threads);
 
 // Kernel variant for x rows per column set and column sets per slice.
 template <int BITS>
@@ -806,12 +804,6 @@ const void *kernel_ptr(int MP, bool db2) {
         default: return nullptr;
     }
 }
-// A small integer naming (bit width, MP, column sets), for per-variant caches.
-inline int variant_id(int bits, int MP, bool db2) {
-    const int mi = MP == 1 ? 0 : (MP == 2 ? 1 : (MP == 4 ? 2 : 3));
-    return (bits * 4 + mi) * 2 + (db2 ? 1 : 0);
-}
-
 template <int BITS>
 LaunchPlan plan_launch(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
                        const uint16_t *bias, uint16_t *y, int M, int K, int N, int group, int F) {
@@ -884,10 +876,10 @@ LaunchPlan plan_launch(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
     if (cudaGetDevice(&dev) != cudaSuccess) return pl;
     const void *fn = kernel_ptr<BITS>(q.MP, q.DB == 2);
     if (fn == nullptr) return pl;
-    if (!set_smem_limit(fn, dev, variant_id(BITS, q.MP, q.DB == 2))) return pl;
+    if (raise_smem_limit(fn, dev, 227 * 1024) != cudaSuccess) return pl;
     const int units = q.tiles / q.unit;
     pl.threads = (q.W + 2) * 32;
-    const int maxc = max_clusters(fn, dev, ks, pl.smem, variant_id(BITS, q.MP, q.DB == 2), pl.threads);
+    const int maxc = max_clusters(fn, dev, ks, pl.smem, pl.threads);
     if (maxc < 1) return pl;
     const int clusters = std::max(1, std::min(units, maxc));
     q.units_base = units / clusters;

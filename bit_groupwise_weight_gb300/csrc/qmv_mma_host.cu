@@ -120,18 +120,7 @@ std::mutex g_spg_mu;
 std::map<std::tuple<int, int, int, int>, int> g_spg_cache;
 
 std::atomic<uint32_t> g_pad_cache[8][8];   // [bits][(crow % 128) / 16]: pad + 1 (0 = unknown)
-std::atomic<int> g_sm_count[64];
-std::atomic<int> g_smem_set[64][64];   // [device][kernel variant]
 
-struct ClusterKey {
-    int dev, bits, ks, threads;
-    uint32_t smem;
-    bool operator<(const ClusterKey &o) const {
-        return std::tie(dev, bits, ks, threads, smem) < std::tie(o.dev, o.bits, o.ks, o.threads, o.smem);
-    }
-};
-std::mutex g_cluster_mu;
-std::map<ClusterKey, int> g_cluster_cache;
 
 }  // namespace
 
@@ -187,63 +176,9 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, uin
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count_dev(int dev) {
-    if (dev < 0 || dev >= 64) return 0;
-    int v = g_sm_count[dev].load(std::memory_order_relaxed);
-    if (v > 0) return v;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 0;
-    g_sm_count[dev].store(v, std::memory_order_relaxed);
-    return v;
-}
-
-bool set_smem_limit(const void *fn, int dev, int variant) {
-    if (dev < 0 || dev >= 64 || variant < 0 || variant >= 64) return false;
-    std::atomic<int> &slot = g_smem_set[dev][variant];
-    if (slot.load(std::memory_order_acquire) == 1) return true;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    slot.store(1, std::memory_order_release);
-    return true;
-}
-
-int max_clusters(const void *fn, int dev, int ks, uint32_t smem, int variant, int threads) {
-    const ClusterKey key{dev, variant, ks, threads, smem};
-    {
-        std::lock_guard<std::mutex> lk(g_cluster_mu);
-        auto it = g_cluster_cache.find(key);
-        if (it != g_cluster_cache.end()) return it->second;
-    }
-    int n = 0;
-    if (ks == 1) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessorWithFlags(&per_sm, fn, threads, smem,
-                                                                   cudaOccupancyDefault) != cudaSuccess) {
-            cudaGetLastError();
-            per_sm = 0;
-        }
-        n = per_sm * sm_count_dev(dev);
-    } else {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(ks);
-        cfg.blockDim = dim3(threads);
-        cfg.dynamicSmemBytes = smem;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = (unsigned)ks;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            n = 0;
-        }
-    }
-    std::lock_guard<std::mutex> lk(g_cluster_mu);
-    g_cluster_cache[key] = n;
-    return n;
+int max_clusters(const void *fn, int dev, int ks, uint32_t smem, int threads) {
+    if (ks == 1) return blocks_per_sm(fn, dev, threads, smem) * device_sm_count(dev);
+    return clusters_at_once(fn, dev, ks, threads, smem);
 }
 
 }  // namespace mma
@@ -263,6 +198,15 @@ cudaError_t launch_qmv_mma(const uint16_t *x, const uint8_t *w, const uint16_t *
         default: return cudaErrorInvalidValue;
     }
 }
+
+bool qmv_mma_shape_ok(int64_t K, int group) {
+    if (K <= 0 || K % mma::kSlice != 0 || K % group != 0 || ((K / group) * 2) % 16 != 0) return false;
+    for (int k = 1; k <= 8; ++k)
+        if (K % (mma::kSlice * k) == 0 && K / k <= mma::kSlice * mma::kMaxW) return true;
+    return false;
+}
+
+int qmv_mma_rows(int group) { return mma::max_rows(group); }
 
 uint32_t mma_timeouts(bool reset) {
     return mma::timeouts_b1(reset) + mma::timeouts_b2(reset) + mma::timeouts_b3(reset) +

@@ -75,6 +75,15 @@ __device__ __forceinline__ uint16_t scale_bits(float mx, float z, float qmax) {
     return __half_as_ushort(__float2half_ru(__double2float_ru(t)));
 }
 
+// fp16 scale of a constant group (every weight equal to mn, all codes 0):
+// the larger of 2^-14 and fp16 rounded toward +inf of 2 (mn - z), so that
+// mn - z <= scale / 2.  mn - z is exact in fp32: z is mn rounded down to fp16,
+// so the two lie within a factor of two, or z is a multiple of mn's ulp.
+__device__ __forceinline__ uint16_t flat_scale_bits(float mn, float z) {
+    const uint32_t cover = __half_as_ushort(__float2half_ru(2.0f * __fsub_rn(mn, z)));
+    return (uint16_t)max(cover, 0x0400u);
+}
+
 // Code of one weight: clamp(rint(fl64(fl64(v - z) / s)), 0, qmax).
 __device__ __forceinline__ uint32_t code_of(float v, float z, float s, float inv_s, float qmax) {
     const float r = __fmul_rn(__fsub_rn(v, z), inv_s);
@@ -171,7 +180,7 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
         // divisions); a group is an aligned run of GL lanes, so a shuffle
         // hands it to the others.
         uint32_t sh32 = 0x0400u;
-        if (!flat && (lane & (GL - 1)) == 0) sh32 = scale_bits(mx, z, qmax);
+        if ((lane & (GL - 1)) == 0) sh32 = flat ? flat_scale_bits(mn, z) : scale_bits(mx, z, qmax);
         const uint16_t sh = (uint16_t)__shfl_sync(0xffffffffu, sh32, lane & ~(GL - 1));
         if (k < K) {
             const float s = __half2float(__ushort_as_half(sh));

@@ -81,7 +81,7 @@ typedef enum {
 /* Which kernel lowbit_linear_ex runs. */
 typedef enum {
     LOWBIT_PATH_AUTO = 0,    /* what lowbit_linear picks (see lowbit_select_path)  */
-    LOWBIT_PATH_QMV = 1,     /* CUDA-core matrix-vector kernel, any M (in chunks)  */
+    LOWBIT_PATH_QMV = 1,     /* decode (matrix-vector) kernels, any M (in chunks)  */
     LOWBIT_PATH_QMM = 2      /* tensor-core (tcgen05) matrix-matrix kernel, any M  */
 } lowbit_path;
 
@@ -128,8 +128,10 @@ LOWBIT_API lowbit_status lowbit_unpack_weights(const uint8_t *packed, uint8_t *c
  *     zero  = fp16 rounded toward -inf of min(w over the group)
  *     scale = fp16 rounded toward +inf of (max - zero) / (2^bits - 1)
  *     q     = clamp(round-half-to-even((w - zero) / scale), 0, 2^bits - 1)
- * and a constant group (max == min) gets scale = 2^-14, q = 0.  Every
- * decision is taken in fp64, so the outputs are fully determined by w.
+ * The minimum of a group holding both signed zeros is the first zero in k
+ * order.  A constant group (max == min) gets q = 0 and scale = the larger of
+ * 2^-14 and fp16 rounded toward +inf of 2 (min - zero).  Every decision is
+ * taken in fp64, so the outputs are fully determined by w.
  * Then |w - (scale*q + zero)| <= scale/2 for every weight.
  *   w        [N, K] of `dtype`, row-major, device, 16-byte aligned.
  *            Values must be finite with magnitude at most 32752, so that a
@@ -192,8 +194,9 @@ LOWBIT_API lowbit_status lowbit_linear_ex(const uint16_t *x, const uint8_t *pack
  * This is the decode step the pages time (torchchat PR #1415 and ao PR #2167
  * measure Llama token generation, whose MLP applies this activation to its
  * gate and up projections); it saves one launch and one pass over a and u.
- * It runs the CUDA-core matrix-vector kernels for every M (rows of x two at a
- * time), so it is meant for decode-sized M.
+ * It runs the decode kernels for every M (up to 8 rows of x per launch on the
+ * tensor-core decode kernel, two on the CUDA-core one), so it is meant for
+ * decode-sized M.
  *   x        [M, K] bf16, as for lowbit_linear.
  *   packed_w [2F, K*bits/8], scales and zeros [2F, K/group], bias NULL or
  *            [2F] fp16: layouts, alignment and ownership as for lowbit_linear
@@ -208,9 +211,15 @@ LOWBIT_API lowbit_status lowbit_linear_swiglu(const uint16_t *x, const uint8_t *
                                    int64_t M, int64_t K, int64_t F, int bits, int group,
                                    lowbit_stream_t stream);
 
-/* The kernel lowbit_linear runs for this problem: LOWBIT_PATH_QMV for small M
- * (decode: M <= 2, or M <= 6 for layers with N >= 9424 outputs) and for K not
- * a multiple of 128, LOWBIT_PATH_QMM above these measured crossovers.
+/* The kernel lowbit_linear runs for this problem, from crossovers measured on
+ * GB300: LOWBIT_PATH_QMV when the tensor-core decode kernel covers M in one
+ * launch (K a multiple of 256 up to 32768 with K/group a multiple of 8:
+ * M <= 2 for group 32, M <= 4 for group 64, M <= 8 for groups 128 and 256),
+ * or in two launches for layers of N >= 20000 outputs; for other K, M <= 2,
+ * or M <= 6 when N >= 9424; and whenever K is not a multiple of 128.
+ * LOWBIT_PATH_QMM otherwise.  The choice assumes x, the packed weights,
+ * scales and zeros 16-byte aligned (the decode path still runs, slower,
+ * when they are not).
  * Host-only; never touches the GPU.  Returns LOWBIT_PATH_AUTO for arguments
  * lowbit_linear would reject. */
 LOWBIT_API lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int group);

@@ -387,7 +387,13 @@ int oracle_silu_mul(const double *y, int64_t M, int64_t F, double *h)
 /*   zero  = fp16 rounded toward -inf of min(w over the group);              */
 /*   scale = fp16 rounded toward +inf of (max - zero) / (2^b - 1);           */
 /*   q     = clamp(round-half-even((w - zero) / scale), 0, 2^b - 1);         */
-/*   a constant group (max == min) gets scale = smallest fp16 normal, q = 0. */
+/*   the minimum of a group holding both zeros is the first zero met in k    */
+/*   order (its sign survives into the zero);                                */
+/*   a constant group (max == min) gets q = 0 and scale = the larger of the  */
+/*   smallest fp16 normal and fp16 rounded toward +inf of 2 (min - zero), so */
+/*   that |w - (scale q + zero)| <= scale / 2 there as everywhere.           */
+/* min - zero is exact in fp64 (zero is min rounded down to fp16, so the two */
+/* lie within a factor of two, or zero is a multiple of min's ulp).          */
 /* ------------------------------------------------------------------------ */
 int oracle_quantize(const double *w, int64_t N, int64_t K, int bits, int group,
                     uint8_t *codes, uint16_t *scales, uint16_t *zeros)
@@ -401,21 +407,35 @@ int oracle_quantize(const double *w, int64_t N, int64_t K, int bits, int group,
             const double *wg = w + n * K + gi * group;
             double mn = wg[0], mx = wg[0];
             for (int i = 1; i < group; ++i) {
+#ifdef PLANT_MIN_LAST
+                if (wg[i] <= mn) mn = wg[i];
+#else
                 if (wg[i] < mn) mn = wg[i];
+#endif
                 if (wg[i] > mx) mx = wg[i];
             }
             uint16_t zh = oracle_double_to_half(mn, ORACLE_RD);
             double z = oracle_half_to_double(zh);
             uint16_t sh;
-            if (mx == mn)
-                sh = 0x0400;                       /* 2^-14 */
-            else
+            if (mx == mn) {
+#ifdef PLANT_CONST_SCALE_FLOOR
+                sh = 0x0400;
+#else
+                uint16_t cover = oracle_double_to_half(2.0 * (mn - z), ORACLE_RU);
+                sh = cover > 0x0400 ? cover : 0x0400;   /* 2^-14 at least */
+#endif
+            } else {
                 sh = oracle_double_to_half((mx - z) / qmax, ORACLE_RU);
+            }
             double s = oracle_half_to_double(sh);
             scales[n * G + gi] = sh;
             zeros[n * G + gi] = zh;
             for (int i = 0; i < group; ++i) {
+#ifdef PLANT_ROUND_HALF_AWAY
+                double q = (mx == mn) ? 0.0 : round((wg[i] - z) / s);
+#else
                 double q = (mx == mn) ? 0.0 : nearbyint((wg[i] - z) / s);
+#endif
                 if (q < 0.0) q = 0.0;
                 if (q > qmax) q = qmax;
                 codes[n * K + gi * group + i] = (uint8_t)q;

@@ -348,14 +348,70 @@ def pin_quantizer_invariant(o):
             assert np.all(s.view(np.float16).astype(np.float64) * ((1 << b) - 1) + zf >= wg.max(axis=2))
 
 
+def _f16_down(v: float) -> float:
+    """Largest fp16 <= v (numpy's float16, stepped down when it rounded up)."""
+    h = np.float16(v)
+    if float(h) > v:
+        h = np.nextafter(h, np.float16(-np.inf))
+    return float(h)
+
+
+def _f16_up(v: float) -> float:
+    """Smallest fp16 >= v."""
+    h = np.float16(v)
+    if float(h) < v:
+        h = np.nextafter(h, np.float16(np.inf))
+    return float(h)
+
+
 def pin_quantizer_constant_group(o):
-    w = np.full((1, 64), 0.3)
-    codes, s, z = o.quantize(w, 4, 32)
-    assert codes.max() == 0
-    assert np.all(s == 0x0400)
-    zf = z.view(np.float16).astype(np.float64)
-    assert np.all(zf <= 0.3) and np.all(np.float16(zf) == np.float16(zf))
-    assert np.all(0.3 - zf < 2.0 ** -11)     # one fp16 ulp at 0.3 is 2^-12
+    # A constant group: every code 0, zero = largest fp16 <= w, scale = the
+    # larger of 2^-14 and the smallest fp16 >= 2 (w - zero), so that the
+    # weight is recovered within scale / 2 even when w is not an fp16 (fp32 or
+    # fp64 input).  Directed rounding here comes from numpy's float16.
+    for v in (0.3, -0.3, 0.1, -1.5, 1000.3, 1e-6, -3e-7, float(np.float32(0.3)),
+              float(np.float32(-7.7)), 0.0, -0.0):
+        for b in (1, 4, 7):
+            codes, s, z = o.quantize(np.full((1, 64), v), b, 32)
+            assert codes.max() == 0
+            zf = _f16_down(v)
+            sf = max(2.0 ** -14, _f16_up(2.0 * (v - zf)))
+            assert np.all(z.view(np.float16).astype(np.float64) == zf), (v, b)
+            assert np.all(s.view(np.float16).astype(np.float64) == sf), (v, b)
+            assert abs(v - zf) <= sf / 2, (v, b)
+            assert np.all(np.signbit(z.view(np.float16)) == np.signbit(zf)), (v, b)
+
+
+def _golden_values(field: str) -> list[float]:
+    out = []
+    for tok in field.split():
+        if "*" in tok:
+            v, n = tok.split("*")
+            out += [float(v)] * int(n)
+        else:
+            out.append(float(tok))
+    return out
+
+
+def pin_quantizer_golden(o):
+    """Hand-derived groups (tests/golden/quantize_worked.txt): exact ties
+    (round half to even), signed-zero minima (first zero in k order) and
+    constant groups, each with its codes, scale and zero worked out by hand."""
+    cases = 0
+    for line in (GOLDEN / "quantize_worked.txt").read_text().splitlines():
+        if not line.strip() or line.startswith("#"):
+            continue
+        bits_f, w_f, q_f, s_f, z_f = (f.strip() for f in line.split(";"))
+        b = int(bits_f)
+        w = np.array(_golden_values(w_f))
+        q = np.array(_golden_values(q_f), dtype=np.int64)
+        assert w.size == 32 and q.size == 32, line[:40]
+        codes, s, z = o.quantize(w[None, :], b, 32)
+        assert codes[0].tolist() == q.tolist(), (line[:40], codes[0].tolist())
+        assert int(s[0, 0]) == int(s_f, 16), (line[:40], hex(int(s[0, 0])))
+        assert int(z[0, 0]) == int(z_f, 16), (line[:40], hex(int(z[0, 0])))
+        cases += 1
+    assert cases == 7
 
 
 def pin_silu_closed_forms(o):
@@ -405,6 +461,6 @@ PINS = [
     pin_half_decode, pin_bf16_decode, pin_half_round,
     pin_linear_worked, pin_linear_integer_matmul, pin_linear_zero_only, pin_linear_one_group,
     pin_linear_bias_and_rows, pin_linear_numpy_matmul, pin_linearity, pin_dequant,
-    pin_quantizer_invariant, pin_quantizer_constant_group,
+    pin_quantizer_invariant, pin_quantizer_constant_group, pin_quantizer_golden,
     pin_silu_closed_forms, pin_silu_odd_identity, pin_silu_layout,
 ]

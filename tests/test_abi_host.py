@@ -68,11 +68,25 @@ def test_select_path(lib):
     assert lb.select_path(1, 4096, 4096, 4, 64) == lb.PATH_QMV
     assert lb.select_path(0, 4096, 4096, 4, 64) == lb.PATH_QMV
     assert lb.select_path(128, 4096, 4096, 4, 64) == lb.PATH_QMM
-    # Measured crossovers: narrow layers (qmm splits K) and wide ones.
-    assert lb.select_path(2, 4096, 4096, 4, 64) == lb.PATH_QMV
-    assert lb.select_path(3, 4096, 4096, 4, 64) == lb.PATH_QMM
-    assert lb.select_path(6, 4096, 28672, 4, 64) == lb.PATH_QMV
-    assert lb.select_path(7, 4096, 28672, 4, 64) == lb.PATH_QMM
+    # Measured crossovers.  The tensor-core decode kernel takes 2 / 4 / 8 rows of x
+    # per launch for g = 32 / 64 / >= 128: one launch always, two only when N >= 20000.
+    assert lb.select_path(4, 4096, 4096, 4, 64) == lb.PATH_QMV
+    assert lb.select_path(5, 4096, 4096, 4, 64) == lb.PATH_QMM
+    assert lb.select_path(8, 4096, 6144, 4, 128) == lb.PATH_QMV
+    assert lb.select_path(9, 4096, 6144, 4, 128) == lb.PATH_QMM
+    assert lb.select_path(8, 14336, 4096, 7, 256) == lb.PATH_QMV
+    assert lb.select_path(2, 4096, 4096, 4, 32) == lb.PATH_QMV
+    assert lb.select_path(3, 4096, 4096, 4, 32) == lb.PATH_QMM
+    assert lb.select_path(16, 4096, 28672, 4, 128) == lb.PATH_QMV
+    assert lb.select_path(17, 4096, 28672, 4, 128) == lb.PATH_QMM
+    assert lb.select_path(16, 4096, 16384, 4, 128) == lb.PATH_QMM
+    # Shapes the decode kernel does not take: the CUDA-core kernel's crossover
+    # (K % 256 != 0; K / group not a multiple of 8).
+    assert lb.select_path(2, 4096 + 128, 4096, 4, 64) == lb.PATH_QMV
+    assert lb.select_path(3, 4096 + 128, 4096, 4, 64) == lb.PATH_QMM
+    assert lb.select_path(6, 4096 + 128, 28672, 4, 64) == lb.PATH_QMV
+    assert lb.select_path(7, 4096 + 128, 28672, 4, 64) == lb.PATH_QMM
+    assert lb.select_path(3, 3072, 3072, 4, 256) == lb.PATH_QMM
     assert lb.select_path(128, 4096 + 64, 4096, 4, 64) == lb.PATH_QMV
     for bad in ((1, 4096, 4096, 0, 64), (1, 4096, 4096, 8, 64), (1, 4096, 4096, 4, 48),
                 (1, 4000, 4096, 4, 64), (1, 0, 4096, 4, 64), (-1, 4096, 4096, 4, 64)):

@@ -122,6 +122,34 @@ def test_linear_decode_tiles_and_chunks(bits, M, K, N, group):
     check_close(y_to_f64(d.run(lb.PATH_QMV)), _oracle_y(L), f"{(M, K, N, bits, group)}")
 
 
+# Rows of x per launch of the tensor-core decode kernel: 2 (g = 32), 4 (g = 64),
+# 8 (g >= 128).  K = 1280 (five 256-code slices, one CTA) and ragged N = 203 take
+# that kernel; M runs through every column-set variant and one launch past the
+# limit (two launches).
+_ROWS = {32: 2, 64: 4, 128: 8, 256: 8}
+
+
+@pytest.mark.parametrize("bits", [1, 3, 4, 7])
+@pytest.mark.parametrize("group", [32, 64, 128, 256])
+def test_decode_kernel_rows_per_launch(bits, group):
+    for M in sorted({1, 2, _ROWS[group] // 2 + 1, _ROWS[group], _ROWS[group] + 1}):
+        L = synth.make_layer(70 + bits + M, M, 1280, 203, bits, group, bias=True, outliers=True)
+        d = DeviceLayer(L)
+        check_close(y_to_f64(d.run(lb.PATH_QMV)), _oracle_y(L), f"M={M} b={bits} g={group}")
+
+
+@pytest.mark.parametrize("M,K,N,bits,group", [
+    (8, 12288, 77, 5, 128),     # K over a cluster of 3 CTAs, eight rows of x
+    (4, 8192, 45, 2, 64),       # cluster of 2, four rows, two column sets
+    (1, 32768, 40, 7, 256),     # the longest K: a cluster of 8
+    (3, 14336, 33, 6, 32),      # g = 32: two launches of the cluster kernel
+])
+def test_decode_kernel_cluster_rows(M, K, N, bits, group):
+    L = synth.make_layer(90 + M + bits, M, K, N, bits, group, bias=True, outliers=True)
+    d = DeviceLayer(L)
+    check_close(y_to_f64(d.run(lb.PATH_QMV)), _oracle_y(L), f"{(M, K, N, bits, group)}")
+
+
 def test_linear_single_qmv_full():
     # K = N = 4096, M = 1, b = 4, g = 64, seed 0: every output.
     L = synth.make_layer(0, **synth.SINGLE_QMV)
@@ -202,7 +230,7 @@ def test_llama8b_int4wo_128(path, M, name):
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 6])
 @pytest.mark.parametrize("group", [32, 64, 128, 256])
-@pytest.mark.parametrize("model,name", [("3B", "qkv"), ("3B", "down"), ("1B", "gate_up"), ("1B", "o")])
+@pytest.mark.parametrize("model,name", [(m, n) for m in ("3B", "1B") for n in synth.LLAMA_3B])
 def test_llama3b1b_decode(bits, group, model, name):
     K, N = (synth.LLAMA_3B if model == "3B" else synth.LLAMA_1B)[name]
     L = synth.make_layer(0, 1, K, N, bits, group)
@@ -255,3 +283,24 @@ def test_auto_path_picks_qmm_for_batches():
 def test_no_wait_timed_out():
     # Every bounded wait in the kernels run above completed in time.
     assert lb.wait_timeouts() == 0
+
+
+def test_second_device_after_first():
+    """Kernel attributes (the raised shared-memory limit) and occupancy are per
+    device: a first call on device 1 after calls on device 0 must still run
+    (both kernels), and agree with device 0 bit for bit."""
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs two GPUs")
+    L = synth.make_layer(5, 8, 1024, 300, 4, 64, bias=True)
+    outs = []
+    for dev in (0, 1):
+        with torch.cuda.device(dev):
+            w = lb.pack_weights(torch.from_numpy(L.codes).cuda(), 4)
+            x = torch.from_numpy(L.x.view(np.int16)).view(torch.bfloat16).cuda()
+            s = torch.from_numpy(L.scales.view(np.int16)).view(torch.float16).cuda()
+            z = torch.from_numpy(L.zeros.view(np.int16)).view(torch.float16).cuda()
+            b = torch.from_numpy(L.bias.view(np.int16)).view(torch.float16).cuda()
+            outs.append([lb.linear(x, w, s, z, b, 4, 64, path=p).cpu() for p in PATHS])
+            torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)

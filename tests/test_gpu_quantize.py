@@ -72,6 +72,12 @@ def _special_groups(bits: int, group: int) -> np.ndarray:
     rows = []
     rows.append(np.full(group, 0.375))                        # constant group
     rows.append(np.full(group, -1.5))                         # constant, negative
+    # Constant groups whose value is not an fp16 (as fp32 input): the scale must
+    # cover min - zero, so that |w - W| <= scale / 2 still holds.
+    rows.append(np.full(group, 0.3))
+    rows.append(np.full(group, -0.3))
+    rows.append(np.full(group, 1000.3))
+    rows.append(np.full(group, 1e-6))
     rows.append(np.zeros(group))                              # all +0
     z = np.zeros(group); z[3] = -0.0; z[5] = 1.0              # +0 first, then -0
     rows.append(z)
@@ -111,9 +117,14 @@ def test_quantize_special_groups(orc, dtype, bits, group):
     w32 = np.ascontiguousarray(np.concatenate([w, w[:, ::-1]], axis=1))
     w_dev, w64 = _as_dtype(w32, dtype)
     # The signed zeros must survive the conversions.
-    assert np.signbit(w64[3, 3]) and not np.signbit(w64[3, 0])
+    assert np.signbit(w64[7, 3]) and not np.signbit(w64[7, 0])
     packed, scales, zeros = _gpu_quantize(w_dev, bits, group)
     _check_exact(orc, w64, packed, scales, zeros, bits, group, f"special {dtype} b={bits} g={group}")
+    # The quantiser's bound, on every weight of every special group.
+    codes = orc.unpack(packed, w64.shape[1], bits).astype(np.float64)
+    sf = np.repeat(scales.view(np.float16).astype(np.float64), group, axis=1)
+    zf = np.repeat(zeros.view(np.float16).astype(np.float64), group, axis=1)
+    assert np.all(np.abs(w64 - (sf * codes + zf)) <= sf / 2), f"bound {dtype} b={bits} g={group}"
 
 
 @pytest.mark.parametrize("bits,group", [(3, 64), (4, 128), (7, 32)])

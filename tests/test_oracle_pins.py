@@ -26,10 +26,13 @@ def test_pin(o, pin):
 # Each planted mistake is a plausible error in reading the pages: the old
 # num_groups x N scale layout, a zero point instead of an additive zero, MSB-first
 # bits, a wrong group index, a dropped term, a transposed operand, a wrong fp16
-# exponent bias, the sign of the exponent in silu, gate and up swapped.
+# exponent bias, the sign of the exponent in silu, gate and up swapped; in the
+# quantiser, ties rounded half away from zero, the last (not the first) of equal
+# minima, and a constant group's scale left at 2^-14.
 PLANTS = ["PLANT_STREAM_MSB", "PLANT_CODE_MSB", "PLANT_GROUP_MOD", "PLANT_SZ_TRANSPOSED",
           "PLANT_DROP_ZERO", "PLANT_ZERO_POINT", "PLANT_DROP_BIAS", "PLANT_X_TRANSPOSED",
-          "PLANT_HALF_BIAS", "PLANT_LAST_K", "PLANT_SILU_SIGN", "PLANT_SILU_SWAP"]
+          "PLANT_HALF_BIAS", "PLANT_LAST_K", "PLANT_SILU_SIGN", "PLANT_SILU_SWAP",
+          "PLANT_ROUND_HALF_AWAY", "PLANT_MIN_LAST", "PLANT_CONST_SCALE_FLOOR"]
 
 
 @pytest.mark.parametrize("plant", PLANTS)
