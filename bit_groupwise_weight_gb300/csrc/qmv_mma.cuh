@@ -266,7 +266,10 @@ struct Params {
     int units_base, units_extra;   // units per cluster: base (+1 for the first `extra`)
     uint32_t row_bytes;  // K * b / 8
     uint32_t crow_bytes; // Kc * b / 8 (one CTA's part of a row)
-    uint32_t sstride;    // shared-memory bytes per staged row (padded)
+    int P;               // parts of a CTA's row range, one TMA box of 16 rows each
+    uint32_t part_bytes; // crow_bytes / P (whole warp slices)
+    uint32_t sstride;    // shared-memory bytes per staged row of a part (padded)
+    uint32_t tile_bytes; // one staged tile: P parts x 16 rows x sstride
     uint32_t sz_off;     // within a stage: scales of its tiles (16 x spg fp16 per tile), then zeros
     uint32_t z_off;
     int spg;             // fp16 per staged row of scales / zeros (a padded box row)
@@ -311,13 +314,9 @@ __device__ __forceinline__ void lds_block_bits(uint32_t addr, uint32_t (&w)[BITS
     }
 }
 
-// First global row of tile lt and its number of valid rows.
+// First global row of tile lt.
 __device__ __forceinline__ int64_t tile_row0(const Params &p, int lt) {
     return p.F == 0 ? (int64_t)lt * kTile : (int64_t)((lt & 1) ? p.F : 0) + (int64_t)(lt >> 1) * kTile;
-}
-__device__ __forceinline__ int tile_rows(const Params &p, int lt) {
-    const int r0 = p.F == 0 ? lt * kTile : (lt >> 1) * kTile;
-    return min(kTile, (p.F == 0 ? p.N : p.F) - r0);
 }
 
 // 8 bf16 of x (16-byte aligned) as fp32.
@@ -377,7 +376,8 @@ __device__ __forceinline__ void red_arrive(bool cluster, uint32_t bar) {
 
 template <int BITS, int MP, bool DB2>
 __global__ void __launch_bounds__(kThreads, 1)
-qmv_mma_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__ CUtensorMap zmap, const Params p) {
+qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap,
+               const __grid_constant__ CUtensorMap zmap, const Params p) {
     static_assert(MP == 1 || MP == 2 || MP == 4 || MP == 8, "rows of x per column set");
     static_assert(!(DB2 && MP == 1), "one row of x always fits one column set");
     constexpr int NB = DB2 ? 2 : 1;                        // column sets per slice
@@ -428,23 +428,25 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__
             const uint32_t full = full0 + 8 * st;
             const uint32_t dst0 = sb + p.ring_off + (uint32_t)st * p.stage_bytes;
             const uint32_t tsz = (uint32_t)(kTile * p.spg * 2);        // bytes of one tile's scales
-            // Scales and zeros: one 2D tensor copy each per tile, a box of 16
-            // rows x spg fp16 from group rank * gcta (rows past the matrix and
-            // columns past its groups read as zero).
-            uint32_t bytes = 0;
-            for (int i = 0; i < nts; ++i) bytes += (uint32_t)tile_rows(p, lta + i) * p.crow_bytes + 2u * tsz;
+            // Weights: one 2D tensor copy per part of a tile, a box of 16 rows
+            // x sstride bytes (8-byte elements) from byte rank * crow + j *
+            // part of the rows: the bytes past the part (the row padding) are
+            // the next part's or next row's, or zeros past the matrix, and
+            // rows past the matrix read as zero.  Scales and zeros: one 2D
+            // tensor copy each per tile, a box of 16 rows x spg fp16 from
+            // group rank * gcta (columns past its groups read as zero).
+            const uint32_t bytes = (uint32_t)nts * (p.tile_bytes + 2u * tsz);
             if (lane == 0) ptx::mbar_arrive_expect_tx(full, bytes);
             __syncwarp();
             for (int i = 0; i < nts; ++i) {
-                const int nr = tile_rows(p, lta + i);
-                const int64_t g0 = tile_row0(p, lta + i);
-                const uint8_t *src = p.w + g0 * p.row_bytes + (int64_t)rank * p.crow_bytes;
-                for (int r = lane; r < nr; r += 32)
-                    ptx::bulk_g2s(dst0 + (uint32_t)(i * kTile + r) * p.sstride, src + (int64_t)r * p.row_bytes,
-                                  p.crow_bytes, full, pol);
+                const int g0 = (int)tile_row0(p, lta + i);
+                if (lane < p.P)
+                    ptx::tma_load_2d_hint(dst0 + (uint32_t)i * p.tile_bytes + (uint32_t)(lane * kTile) * p.sstride,
+                                          &wmap, (int)((rank * p.crow_bytes + (uint32_t)lane * p.part_bytes) >> 3),
+                                          g0, full, pol);
                 if (lane == 31) {
-                    ptx::tma_load_2d_hint(dst0 + p.sz_off + i * tsz, &smap, rank * p.gcta, (int)g0, full, pol);
-                    ptx::tma_load_2d_hint(dst0 + p.z_off + i * tsz, &zmap, rank * p.gcta, (int)g0, full, pol);
+                    ptx::tma_load_2d_hint(dst0 + p.sz_off + i * tsz, &smap, rank * p.gcta, g0, full, pol);
+                    ptx::tma_load_2d_hint(dst0 + p.z_off + i * tsz, &zmap, rank * p.gcta, g0, full, pol);
                 }
             }
         }
@@ -629,15 +631,17 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__
         }
 
         // Shared-memory byte offsets, fixed per thread: row gid's first block
-        // within a staged tile, row gid + 8 from there, a tile's stride; the
+        // within a staged tile (the warp's slice lies in part warp / (W / P)),
+        // row gid + 8 from there, a tile's stride; the
         // scales of rows gid and gid + 8 within a tile's scale box (the zeros
         // sit zdelta bytes after their scales); this thread's slot in a
         // reduction buffer of the cluster's first CTA (this CTA's own when
         // there is no cluster).
-        const uint32_t a_off = (uint32_t)gid * p.sstride + (uint32_t)warp * (kSlice * BITS / 8) +
-                               (uint32_t)((32 * t * BITS) >> 3);
+        const int wpp = W / p.P;                                  // warps per part
+        const uint32_t a_off = (uint32_t)((warp / wpp) * kTile + gid) * p.sstride +
+                               (uint32_t)(warp % wpp) * (kSlice * BITS / 8) + (uint32_t)((32 * t * BITS) >> 3);
         const uint32_t b_off = 8u * p.sstride;
-        const uint32_t t_str = (uint32_t)kTile * p.sstride;
+        const uint32_t t_str = p.tile_bytes;
         const uint32_t tsz = (uint32_t)(kTile * p.spg * 2);
         const uint32_t zdelta = p.z_off - p.sz_off;
         const uint32_t r8 = (uint32_t)(16 * p.spg);                      // 8 scale rows, bytes
@@ -768,7 +772,7 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__
 struct LaunchPlan {
     bool ok = false;
     Params prm{};
-    CUtensorMap smap, zmap;
+    CUtensorMap wmap, smap, zmap;
     int grid = 0;
     int threads = 0;
     uint32_t smem = 0;
@@ -832,7 +836,20 @@ LaunchPlan plan_launch(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
     q.tiles = F != 0 ? 2 * (F / kTile) : (N + kTile - 1) / kTile;
     q.row_bytes = (uint32_t)((int64_t)K * BITS / 8);
     q.crow_bytes = (uint32_t)((int64_t)q.Kc * BITS / 8);
-    q.sstride = q.crow_bytes + row_pad(BITS, q.crow_bytes);
+    // A part of a CTA's row range is whole warp slices and, with its padding,
+    // fits one TMA box row (at most 256 elements of 8 bytes): the fewest parts.
+    for (int pp = 1; pp <= q.W && q.P == 0; ++pp) {
+        if (q.W % pp != 0) continue;
+        const uint32_t part = q.crow_bytes / (uint32_t)pp;
+        const uint32_t pad = row_pad(BITS, part);
+        if (part + pad <= 256u * 8u) {
+            q.P = pp;
+            q.part_bytes = part;
+            q.sstride = part + pad;
+        }
+    }
+    if (q.P == 0) return pl;
+    q.tile_bytes = (uint32_t)q.P * kTile * q.sstride;
     // Scales and zeros: a CTA fetches its own groups when they start on a
     // 16-byte boundary, else whole rows; the box row is padded (over-read)
     // so that the epilogue's reads of 16 rows fall into distinct banks.
@@ -844,7 +861,7 @@ LaunchPlan plan_launch(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
     constexpr uint32_t kBudget = 227u * 1024u;
     constexpr uint32_t kBars = 16u * kMaxStages + 16u * kRedBufs;
     for (int rs = 8; rs >= q.unit; rs -= q.unit) {
-        const uint32_t stage = (uint32_t)rs * kTile * (q.sstride + 4u * (uint32_t)q.spg);
+        const uint32_t stage = (uint32_t)rs * (q.tile_bytes + kTile * 4u * (uint32_t)q.spg);
         if (rs > q.unit && stage > 72u * 1024u) continue;
         const uint32_t red_floats = (uint32_t)(ks * q.W * rs * kTile * q.MP);
         const uint32_t red_off = (kBars + 127u) & ~127u;
@@ -856,7 +873,7 @@ LaunchPlan plan_launch(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
         q.RS = rs;
         q.NS = ns;
         q.stage_bytes = stage;
-        q.sz_off = (uint32_t)rs * kTile * q.sstride;
+        q.sz_off = (uint32_t)rs * q.tile_bytes;
         q.z_off = q.sz_off + (uint32_t)rs * kTile * (uint32_t)q.spg * 2u;
         q.red_floats = red_floats;
         q.red_off = red_off;
@@ -867,7 +884,9 @@ LaunchPlan plan_launch(const uint16_t *x, const uint8_t *w, const uint16_t *s, c
     }
     if (q.RS == 0) return pl;
     const int rows_total = F != 0 ? 2 * F : N;
-    if (!encode_2d(&pl.smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, s, (uint64_t)q.G, (uint64_t)rows_total,
+    if (!encode_2d(&pl.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, w, (uint64_t)(q.row_bytes / 8u), (uint64_t)rows_total,
+                   (uint64_t)q.row_bytes, q.sstride / 8u, kTile) ||
+        !encode_2d(&pl.smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, s, (uint64_t)q.G, (uint64_t)rows_total,
                    (uint64_t)q.G * 2, (uint32_t)q.spg, kTile) ||
         !encode_2d(&pl.zmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, z, (uint64_t)q.G, (uint64_t)rows_total,
                    (uint64_t)q.G * 2, (uint32_t)q.spg, kTile))
@@ -905,10 +924,10 @@ cudaError_t launch_plan(const LaunchPlan &pl, cudaStream_t stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pl.prm.ks > 1 ? 2 : 1;
-    using KFn = void (*)(const CUtensorMap, const CUtensorMap, const Params);
+    using KFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params);
     const KFn fn = reinterpret_cast<KFn>(const_cast<void *>(kernel_ptr<BITS>(pl.prm.MP, pl.prm.DB == 2)));
     if (fn == nullptr) return cudaErrorInvalidValue;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, pl.smap, pl.zmap, pl.prm);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, pl.wmap, pl.smap, pl.zmap, pl.prm);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
