@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <utility>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -149,6 +150,12 @@ int device_sm_count(int dev);
 cudaError_t raise_smem_limit(const void *fn, int dev, int bytes);       // once per (device, kernel, bytes)
 int blocks_per_sm(const void *fn, int dev, int threads, uint32_t smem);
 int clusters_at_once(const void *fn, int dev, int ks, int threads, uint32_t smem);
+// A TMA tiled tensor map (element strides 1, no interleave, L2 promotion 256 B,
+// out-of-bounds elements read as zero): rank dims (innermost first), rank - 1
+// byte strides, the box.  Cached by its arguments.  False when encoding fails.
+bool encode_tiled(CUtensorMap *map, CUtensorMapDataType type, uint32_t rank, const void *base,
+                  const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
+                  CUtensorMapSwizzle swizzle);
 // True when the tensor-core decode kernel takes K and group (given 16-byte
 // aligned x, weights, scales and zeros), and the rows of x it takes per launch.
 bool qmv_mma_shape_ok(int64_t K, int group);

@@ -495,26 +495,10 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
 // Host side.
 // ---------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static std::atomic<void *> fn{nullptr};
-    void *f = fn.load(std::memory_order_acquire);
-    if (f == nullptr) {
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn.store(f, std::memory_order_release);
-    }
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-}
-
 template <int BITS>
 cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, const uint16_t *z,
                         const uint16_t *bias, uint16_t *y, int M, int K, int N, int group,
                         cudaStream_t stream) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (enc == nullptr) return cudaErrorNotSupported;
     QmmParams q{};
     q.s = s; q.z = z; q.bias = bias; q.y = y;
     q.M = M; q.N = N; q.K = K; q.G = K / group; q.log2g = __builtin_ctz((unsigned)group);
@@ -541,24 +525,18 @@ cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, 
 
     CUtensorMap xmap, wmap;
     {
-        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {64, (cuuint32_t)q.TN};
-        const cuuint32_t estr[2] = {1, 1};
-        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box,
-                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+        const uint64_t strides[1] = {(uint64_t)K * 2};
+        const uint32_t box[2] = {64, (uint32_t)q.TN};
+        if (!encode_tiled(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
     {
-        const cuuint64_t row_bytes = (cuuint64_t)K * BITS / 8;
-        const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)N};
-        const cuuint64_t strides[1] = {row_bytes};
-        const cuuint32_t box[2] = {(cuuint32_t)(kBK * BITS / 8), (cuuint32_t)kBM};
-        const cuuint32_t estr[2] = {1, 1};
-        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(w), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        const uint64_t row_bytes = (uint64_t)K * BITS / 8;
+        const uint64_t dims[2] = {row_bytes, (uint64_t)N};
+        const uint64_t strides[1] = {row_bytes};
+        const uint32_t box[2] = {(uint32_t)(kBK * BITS / 8), (uint32_t)kBM};
+        if (!encode_tiled(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
     const void *kfn = reinterpret_cast<const void *>(&qmm_kernel<BITS>);

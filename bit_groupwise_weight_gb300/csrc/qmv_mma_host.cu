@@ -102,20 +102,6 @@ int sz_model(int spg, int gsl, int MP, int W) {
     return total;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_entry() {
-    static std::atomic<void *> fn{nullptr};
-    void *f = fn.load(std::memory_order_acquire);
-    if (f == nullptr) {
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn.store(f, std::memory_order_release);
-    }
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-}
-
 std::mutex g_spg_mu;
 std::map<std::tuple<int, int, int, int>, int> g_spg_cache;
 
@@ -165,15 +151,10 @@ int sz_pitch(int groups, int gsl, int MP, int W) {
 
 bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, uint64_t inner, uint64_t rows,
                uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_entry();
-    if (enc == nullptr) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)row_stride_bytes};
-    const cuuint32_t box[2] = {box_inner, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, type, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const uint64_t dims[2] = {inner, rows};
+    const uint64_t strides[1] = {row_stride_bytes};
+    const uint32_t box[2] = {box_inner, box_rows};
+    return encode_tiled(map, type, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 int max_clusters(const void *fn, int dev, int ks, uint32_t smem, int threads) {
