@@ -363,6 +363,21 @@ __device__ __forceinline__ void tile_block(uint32_t rowa, uint32_t rowb, const u
     }(std::make_integer_sequence<int, 8>{});
 }
 
+// Sum of the nsrc partials of one output (stride `step` floats in the
+// reduction buffer) as eight independent chains combined in a fixed order:
+// the result is the same on every call, and the loads are not serialised
+// behind the adds (a cluster of 8 CTAs has up to 128 partials per output).
+__device__ __forceinline__ float sum_partials(const float *red, int nsrc, int step) {
+    float c[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int src = 0;
+    for (; src + 8 <= nsrc; src += 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c[j] += red[(src + j) * step];
+    }
+    for (; src < nsrc; ++src) c[0] += red[src * step];
+    return ((c[0] + c[1]) + (c[2] + c[3])) + ((c[4] + c[5]) + (c[6] + c[7]));
+}
+
 // Bounded waits and arrivals on the reduction barriers: cluster scope when
 // the K range is split over a cluster, CTA scope (no fence) otherwise.
 __device__ __forceinline__ bool red_wait(bool cluster, uint32_t bar, uint32_t parity) {
@@ -471,8 +486,7 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
                         const int rr = o / MP, m = o % MP;
                         const int row = (lta + rr / kTile) * kTile + rr % kTile;
                         if (m < p.M && row < p.N) {
-                            float a = 0.f;
-                            for (int src = 0; src < nsrc; ++src) a += red[(src * rows_stage + rr) * MP + m];
+                            float a = sum_partials(red + rr * MP + m, nsrc, rows_stage * MP);
                             if (p.bias != nullptr) a += half_bits_to_float(p.bias[row]);
                             p.y[(int64_t)m * p.N + row] = float_to_bf16_bits(a);
                         }
@@ -485,11 +499,8 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
                         const int f = ((lta >> 1) + ip) * kTile + r;
                         if (m < p.M && f < p.F) {
                             const int ra = (2 * ip) * kTile + r, ru = ra + kTile;
-                            float a = 0.f, u = 0.f;
-                            for (int src = 0; src < nsrc; ++src) {
-                                a += red[(src * rows_stage + ra) * MP + m];
-                                u += red[(src * rows_stage + ru) * MP + m];
-                            }
+                            float a = sum_partials(red + ra * MP + m, nsrc, rows_stage * MP);
+                            float u = sum_partials(red + ru * MP + m, nsrc, rows_stage * MP);
                             if (p.bias != nullptr) {
                                 a += half_bits_to_float(p.bias[f]);
                                 u += half_bits_to_float(p.bias[p.F + f]);
