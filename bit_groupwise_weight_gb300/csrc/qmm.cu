@@ -65,9 +65,10 @@ constexpr int kAStages = 2;          // code tiles in tensor memory
 constexpr int kACols = kBK / 2;      // TMEM columns of one code tile (two bf16 per column)
 constexpr int kUnpackWarps = 4;      // one per TMEM lane quarter
 constexpr int kAccWarps = 8;
-constexpr int kFirstUnpackWarp = 2;
-constexpr int kFirstAccWarp = kFirstUnpackWarp + kUnpackWarps;    // 6
-constexpr int kThreads = (kFirstAccWarp + kAccWarps) * 32;        // 448
+constexpr int kIssuers = 2;          // MMA-issuing threads (warps 1 and 2, lane 0)
+constexpr int kFirstUnpackWarp = 1 + kIssuers;                    // 3
+constexpr int kFirstAccWarp = kFirstUnpackWarp + kUnpackWarps;    // 7
+constexpr int kThreads = (kFirstAccWarp + kAccWarps) * 32;        // 480
 constexpr int kMaxTmemBufs = 4;
 constexpr uint32_t kBf16Magic = 0x43004300u;                      // bf16 pair (128, 128)
 
@@ -149,6 +150,70 @@ __device__ __forceinline__ void lds_words(const uint8_t *p, uint32_t (&w)[BITS])
 #pragma unroll
         for (int i = 0; i < BITS; ++i) w[i] = reinterpret_cast<const uint32_t *>(p)[i];
     }
+}
+
+// What an MMA-issuing thread needs (shared addresses of the barriers, tensor
+// memory, descriptors).
+struct IssueCtx {
+    uint32_t tmem, a_tmem;
+    uint32_t x_full, a_full, t_full, t_empty, x_empty, a_empty;
+    uint64_t xd0;                     // descriptor of x stage 0
+    uint32_t xd_stage, xd_atom;       // descriptor address units: next stage, second 64-code half
+    uint32_t idesc;
+    int nkt, nbuf, TN;
+};
+
+// Issues the MMAs of K steps me, me + nis, me + 2 nis, ... of this CTA (SPS
+// segments of 128 / SPS codes per step, each into the next accumulator
+// buffer).  Returns false after a wait timed out.
+//
+// One thread issuing every step keeps the tensor core only ~65% busy: any
+// instruction between a step's MMAs (barrier waits, buffer bookkeeping) idles
+// it, because it holds only a couple of MMAs in its queue.  With two threads
+// taking alternate steps, one issues while the other waits, and the MMAs of
+// consecutive steps (different buffers, stages and barriers) interleave
+// freely.  Two issuers need SPS = 1 and at least two buffers: then every
+// barrier phase a thread waits for is at most one behind the one it last saw
+// itself, so parity waits cannot alias.
+template <int SPS>
+__device__ __forceinline__ bool issue_steps(const IssueCtx &c, int me, int nis) {
+    constexpr int kPer = (kBK / 16) / SPS;       // MMAs per segment
+    int b = (me * SPS) % c.nbuf;                 // buffer of this thread's next segment
+    int r = (me * SPS) / c.nbuf;                 // how often that buffer was used before
+    for (int kt = me; kt < c.nkt; kt += nis) {
+        const int st = kt & (kXStages - 1), as = kt & (kAStages - 1);
+        if (!ptx::mbar_wait(c.x_full + 8 * st, (kt / kXStages) & 1, &g_qmm_timeouts) ||
+            !ptx::mbar_wait(c.a_full + 8 * as, (kt / kAStages) & 1, &g_qmm_timeouts))
+            return false;
+        const uint32_t a_st = c.a_tmem + (uint32_t)(as * kACols);
+        const uint64_t xd = c.xd0 + (uint64_t)st * c.xd_stage;
+#pragma unroll
+        for (int j = 0; j < SPS; ++j) {
+            if (r > 0 && !ptx::mbar_wait(c.t_empty + 8 * b, (uint32_t)(r - 1) & 1u, &g_qmm_timeouts)) return false;
+            ptx::tc_fence_after();
+            const uint32_t d = c.tmem + (uint32_t)(b * c.TN);
+#pragma unroll
+            for (int m = 0; m < kPer; ++m) {
+                const int kk = j * kPer + m;
+                ptx::mma_f16_tmem_a(d, a_st + (uint32_t)(kk * 8),
+                                    xd + (uint64_t)((kk >> 2) * c.xd_atom + (kk & 3) * 2), c.idesc, m != 0);
+            }
+            ptx::mma_commit(c.t_full + 8 * b);
+            if (++b == c.nbuf) {
+                b = 0;
+                ++r;
+            }
+        }
+        ptx::mma_commit(c.x_empty + 8 * st);
+        ptx::mma_commit(c.a_empty + 8 * as);
+        for (int i = 0; i < (nis - 1) * SPS; ++i) {      // the other issuers' segments
+            if (++b == c.nbuf) {
+                b = 0;
+                ++r;
+            }
+        }
+    }
+    return true;
 }
 
 // Final rows of one accumulating thread: y[m, n] = acc + bias for its chunks
@@ -249,7 +314,6 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
     const uint32_t a_tmem = tmem + (uint32_t)p.a_col;    // code tiles: kAStages x kACols columns
     const uint32_t x_base = base + p.x_off;
     const uint32_t p_base = base + p.p_off;
-    const int lseg = 1 << p.lseg_log2;           // codes per segment (min(g, 128))
     const int sps = kBK >> p.lseg_log2;          // segments per stage
 
     if (warp == 0) {
@@ -279,56 +343,29 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
             for (int i = max(0, issued - depth); i < issued; ++i)
                 if (!ptx::mbar_wait(full + 8 * (i % depth), (i / depth) & 1, &g_qmm_timeouts)) break;
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer.
+    } else if (warp < kFirstUnpackWarp) {
+        // ---------------- MMA issuers (lane 0 of warps 1 and 2).
         if (lane == 0) {
-            // The tensor core queues only a few MMAs (an MMA completes about
-            // 400 cycles after it is issued), so any slow instruction between
-            // two MMAs idles it.  The stage's eight MMAs are therefore unrolled
-            // with operand addresses formed by adds, and ring and buffer
-            // indices advance by counters instead of divisions.
             static_assert((kXStages & (kXStages - 1)) == 0 && (kAStages & (kAStages - 1)) == 0 && kBK == 128,
                           "ring shapes");
-            const uint32_t idesc = p.idesc;
-            const int mmask = (lseg >> 4) - 1;            // MMAs per segment - 1 (7, 3 or 1)
-            const uint64_t xd0 = ptx::sw128_desc(x_base);
-            const uint64_t xd_stage = p.x_stage >> 4, xd_atom = p.x_stage >> 5;   // descriptor address units
-            int b = 0;                                    // TMEM buffer of the current segment
-            uint32_t tpar = 0;                            // parity of its t_empty wait (round r >= 1: (r - 1) & 1)
-            bool reuse = false;                           // buffers have all been used once
-            bool ok = true;
-            for (int kt = 0; kt < nkt && ok; ++kt) {          // kt relative to kt0 here
-                const int st = kt & (kXStages - 1), as = kt & (kAStages - 1);
-                ok = ptx::mbar_wait(x_full + 8 * st, (kt / kXStages) & 1, &g_qmm_timeouts) &&
-                     ptx::mbar_wait(a_full + 8 * as, (kt / kAStages) & 1, &g_qmm_timeouts);
-                if (!ok) break;
-                const uint32_t a_st = a_tmem + (uint32_t)(as * kACols);
-                const uint64_t xd = xd0 + (uint64_t)st * xd_stage;
-                uint32_t d = tmem;
-#pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    if ((kk & mmask) == 0) {
-                        if (reuse && !ptx::mbar_wait(t_empty + 8 * b, tpar, &g_qmm_timeouts)) {
-                            ok = false;
-                            break;
-                        }
-                        ptx::tc_fence_after();
-                        d = tmem + (uint32_t)(b * p.TN);
-                    }
-                    ptx::mma_f16_tmem_a(d, a_st + (uint32_t)(kk * 8), xd + (uint64_t)((kk >> 2) * xd_atom + (kk & 3) * 2),
-                                        idesc, (kk & mmask) != 0);
-                    if ((kk & mmask) == mmask) {
-                        ptx::mma_commit(t_full + 8 * b);
-                        if (++b == p.nbuf) {
-                            b = 0;
-                            if (reuse) tpar ^= 1u;
-                            reuse = true;
-                        }
-                    }
-                }
-                if (!ok) break;
-                ptx::mma_commit(x_empty + 8 * st);
-                ptx::mma_commit(a_empty + 8 * as);
+            IssueCtx c;
+            c.tmem = tmem;
+            c.a_tmem = a_tmem;
+            c.x_full = x_full; c.a_full = a_full; c.t_full = t_full; c.t_empty = t_empty;
+            c.x_empty = x_empty; c.a_empty = a_empty;
+            c.xd0 = ptx::sw128_desc(x_base);
+            c.xd_stage = p.x_stage >> 4;
+            c.xd_atom = p.x_stage >> 5;
+            c.idesc = p.idesc;
+            c.nkt = nkt;
+            c.nbuf = p.nbuf;
+            c.TN = p.TN;
+            const int me = warp - 1;
+            if (sps == 1) {
+                issue_steps<1>(c, me, kIssuers);
+            } else if (me == 0) {
+                if (sps == 2) issue_steps<2>(c, 0, 1);
+                else issue_steps<4>(c, 0, 1);
             }
         }
     } else if (warp < kFirstAccWarp) {
