@@ -85,7 +85,7 @@ struct QmmParams {
     int kt_unit;            // K tiles per split unit (a group spans whole units)
     uint32_t recv_off;      // split-K: partial sums from the other CTAs (from base)
     uint32_t x_stage;       // TN * kBK * 2 bytes (two swizzle atoms of TN rows)
-    uint32_t x_off, p_off, xs_off;   // offsets from the 1024-aligned base
+    uint32_t x_off, p_off;           // offsets from the 1024-aligned base
     uint32_t idesc;         // tcgen05 instruction descriptor
 };
 
@@ -369,9 +369,12 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
             }
         }
     } else if (warp < kFirstAccWarp) {
-        // ---------------- code unpackers (warps 2..5): thread = one tile row = its TMEM lane.
+        // ---------------- code unpackers (warps 3..6): thread = one tile row = its TMEM lane.
         const int q = warp & 3;
-        const int pr = q * 31 + lane;                    // packed row in the tile (lane 31: ones row)
+        // Packed row of this lane in the tile; lane 31 holds the ones row and
+        // reads the next quarter's first row (in the tile) only to keep the
+        // warp converged.
+        const int pr = q * 31 + lane;
         const uint32_t trow = ((uint32_t)(q * 32) << 16);
         bool ok = true;
         for (int kt = 0; kt < nkt && ok; ++kt) {              // kt relative to kt0 here
@@ -383,19 +386,19 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
             ptx::tc_fence_after();
             const uint8_t *pk = smem + p.p_off + st * kPackedStage + pr * (kBK * BITS / 8);
             const uint32_t adst = a_tmem + trow + (uint32_t)(as * kACols);
+            // All four 32-code blocks are loaded before the first tensor-memory
+            // store, so that one shared-memory latency covers the step.
+            uint32_t w[4][BITS];
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) lds_words<BITS>(pk + blk * (4 * BITS), w[blk]);
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
                 uint32_t h[16];
-                if (lane < 31) {
-                    uint32_t w[BITS];
-                    lds_words<BITS>(pk + blk * (4 * BITS), w);
-                    [&]<int... J>(std::integer_sequence<int, J...>) {
-                        ((h[J] = code_pair<BITS, J>(w)), ...);
-                    }(std::make_integer_sequence<int, 16>{});
-                } else {
+                [&]<int... J>(std::integer_sequence<int, J...>) {
+                    ((h[J] = code_pair<BITS, J>(w[blk])), ...);
+                }(std::make_integer_sequence<int, 16>{});
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) h[j] = 0x3F803F80u;   // bf16 (1, 1)
-                }
+                for (int j = 0; j < 16; ++j) h[j] = lane == 31 ? 0x3F803F80u : h[j];   // bf16 (1, 1)
                 ptx::tmem_st16(adst + (uint32_t)(blk * 16), h);
             }
             ptx::tmem_st_wait();
@@ -407,14 +410,12 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
             }
         }
     } else {
-        // ---------------- accumulators (warps 8..15).
+        // ---------------- accumulators (warps 7..14).
         const int q = warp & 3;                          // tensor-memory lane quarter
         const int h = (warp - kFirstAccWarp) >> 2;       // which half of the 16-column chunks
         const int n = n0 + q * 31 + lane;                // TMEM lane 32q + lane; lane 31 is a ones row
         const bool row_ok = lane < 31 && n < p.N;
         const int nrow = min(n, p.N - 1);
-        // Warp-private slot for lane 31's group sums (32 floats).
-        float *xw = reinterpret_cast<float *>(smem + p.xs_off) + (warp - kFirstAccWarp) * 32;
         const int nchunk = p.TN / 16;
         float2 acc[4][8];                                // chunks h, h+2, h+4, h+6
 #pragma unroll
@@ -459,35 +460,22 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
                     if (lane == 0) ptx::mbar_arrive(t_empty + 8 * b);
                     released = true;
                 }
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int ch = h + 2 * (c2 + u);
-                    if (ch < nchunk) {
-                        if (lane == 31) {
-#pragma unroll
-                            for (int j = 0; j < 16; j += 4)
-                                *reinterpret_cast<uint4 *>(xw + u * 16 + j) =
-                                    make_uint4(v[u][j], v[u][j + 1], v[u][j + 2], v[u][j + 3]);
-                        }
-                    }
-                }
-                __syncwarp();
+                // The group sums X_g of the chunk's columns sit in lane 31 (the
+                // ones row) and are broadcast by shuffles.
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int ch = h + 2 * (c2 + u);
                     if (ch < nchunk) {
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float4 xg = *reinterpret_cast<const float4 *>(xw + u * 16 + j);
-                            float2 &a0 = acc[c2 + u][j / 2], &a1 = acc[c2 + u][j / 2 + 1];
-                            ptx::ffma2(a0, make_float2(__uint_as_float(v[u][j]), __uint_as_float(v[u][j + 1])), s2, a0);
-                            ptx::ffma2(a1, make_float2(__uint_as_float(v[u][j + 2]), __uint_as_float(v[u][j + 3])), s2, a1);
-                            ptx::ffma2(a0, make_float2(xg.x, xg.y), z2, a0);
-                            ptx::ffma2(a1, make_float2(xg.z, xg.w), z2, a1);
+                        for (int j = 0; j < 16; j += 2) {
+                            const float x0 = __shfl_sync(0xFFFFFFFFu, __uint_as_float(v[u][j]), 31);
+                            const float x1 = __shfl_sync(0xFFFFFFFFu, __uint_as_float(v[u][j + 1]), 31);
+                            float2 &a = acc[c2 + u][j / 2];
+                            ptx::ffma2(a, make_float2(__uint_as_float(v[u][j]), __uint_as_float(v[u][j + 1])), s2, a);
+                            ptx::ffma2(a, make_float2(x0, x1), z2, a);
                         }
                     }
                 }
-                __syncwarp();                            // xw is reused by the next pair of chunks
             }
         }
         if (ks == 1) {
@@ -549,8 +537,7 @@ cudaError_t launch_bits(const uint16_t *x, const uint8_t *w, const uint16_t *s, 
     q.nseg = K >> q.lseg_log2;
     q.x_stage = (uint32_t)q.TN * kBK * 2u;
     const uint32_t packed = kBM * (kBK * BITS / 8);
-    q.xs_off = 512;                                   // 8 warps x 32 fp32 group sums
-    q.x_off = 2048;
+    q.x_off = 1024;                                   // after the barriers
     q.p_off = q.x_off + kXStages * q.x_stage;
     const uint32_t budget = 226u * 1024u - 1024u;     // minus alignment slack
     q.pstages = (int)std::min<uint32_t>(kMaxPStages, (budget - q.p_off) / packed);
