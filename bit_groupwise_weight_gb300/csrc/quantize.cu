@@ -13,13 +13,19 @@
 // reaches the same bits with fp32 arithmetic wherever fp32 provably decides
 // the same way, and falls back to fp64 where it cannot tell:
 //   - min and max are exact in fp32 (the inputs are fp32, bf16 or fp16);
-//   - the fp64 scale quotient lies between the fp32 quotients rounded down
-//     and up, so when both round up to the same fp16 that fp16 is the scale;
+//   - the fp64 scale quotient lies between (max - zero) rounded down times
+//     1/qmax rounded down, and the same rounded up (every step rounded
+//     outward), so when both bounds round up to the same fp16 that fp16 is
+//     the scale (the fp64 quotient is the fp64 value nearest the exact one,
+//     and no fp32 bound can lie between the two);
 //   - (w - zero) / scale in fp32 differs from the fp64 quotient by less than
 //     3 * 2^-24 * 2^7 < 2^-15 (it is at most 2^7 and carries three roundings
 //     of 2^-24 relative), so its round-half-even agrees with fp64's unless it
 //     lies within that distance of a half-integer; codes within 2^-14 of one
 //     are recomputed in fp64.
+// The codes need no clamping: zero <= min and scale >= (max - zero) / qmax,
+// so the exact quotient lies in [0, qmax], and the fp32 and fp64 quotients
+// stay within [0, qmax + 2^-15].
 // The codes are written packed (contiguous, LSB-first, ao PR #2167 Summary
 // bullet 2).
 //
@@ -64,10 +70,17 @@ __device__ __forceinline__ W8 load8(const void *w, int dtype, int64_t k0) {
     return r;
 }
 
-// fp16 scale: rounded toward +inf of fl64(fl64(mx - z) / qmax).
-__device__ __forceinline__ uint16_t scale_bits(float mx, float z, float qmax) {
-    const uint16_t lo = __half_as_ushort(__float2half_ru(__fdiv_rd(__fsub_rd(mx, z), qmax)));
-    const uint16_t hi = __half_as_ushort(__float2half_ru(__fdiv_ru(__fsub_ru(mx, z), qmax)));
+// fp16 scale: rounded toward +inf of fl64(fl64(mx - z) / qmax).  rq_lo and
+// rq_hi are 1/qmax rounded down and up.  The bounds from the reciprocal are
+// cheap but a little wider than those of directed divisions, which also
+// decide the common case of an exact quotient; fp64 decides the rest.
+__device__ __forceinline__ uint16_t scale_bits(float mx, float z, float qmax, float rq_lo, float rq_hi) {
+    const float d_lo = __fsub_rd(mx, z), d_hi = __fsub_ru(mx, z);
+    uint16_t lo = __half_as_ushort(__float2half_ru(__fmul_rd(d_lo, rq_lo)));
+    uint16_t hi = __half_as_ushort(__float2half_ru(__fmul_ru(d_hi, rq_hi)));
+    if (lo == hi) return lo;
+    lo = __half_as_ushort(__float2half_ru(__fdiv_rd(d_lo, qmax)));
+    hi = __half_as_ushort(__float2half_ru(__fdiv_ru(d_hi, qmax)));
     if (lo == hi) return lo;
     const double t = ((double)mx - (double)z) / (double)qmax;
     // Directed rounding to fp16 through fp32 in the same direction equals
@@ -84,15 +97,53 @@ __device__ __forceinline__ uint16_t flat_scale_bits(float mn, float z) {
     return (uint16_t)max(cover, 0x0400u);
 }
 
-// Code of one weight: clamp(rint(fl64(fl64(v - z) / s)), 0, qmax).
-__device__ __forceinline__ uint32_t code_of(float v, float z, float s, float inv_s, float qmax) {
-    const float r = __fmul_rn(__fsub_rn(v, z), inv_s);
-    float q = rintf(r);
-    // |r - q| is exact and at most 1/2; within 2^-14 of 1/2 the fp32 quotient
-    // cannot decide the rounding, fp64 does.
-    if (fabsf(__fsub_rn(r, q)) > 0.5f - 1.0f / 16384.0f)
-        q = (float)rint(((double)v - (double)z) / (double)s);
-    return (uint32_t)fminf(fmaxf(q, 0.0f), qmax);
+// Packed fp32 pairs (IEEE round-to-nearest, subnormals kept).
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    unsigned long long r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
+    return *reinterpret_cast<float2 *>(&r);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
+    return *reinterpret_cast<float2 *>(&r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
+    return *reinterpret_cast<float2 *>(&r);
+}
+
+// Codes of a lane's 8 weights: rint(fl64(fl64(v - z) / s)) (see the header).
+// r = (v - z) * (1/s) in fp32; t = r + 2^23 rounds r to the nearest integer,
+// ties to even, into t's low mantissa bits (0 <= r < 2^22), so t's bits are
+// 0x4B000000 + code; r - (t - 2^23) is exact.  Weights whose r lies within
+// 2^-14 of a half-integer are recomputed in fp64.
+__device__ __forceinline__ void codes8(const float (&v)[8], float z, float s, float inv_s, uint32_t (&q)[8]) {
+    const float2 z2 = make_float2(z, z), is2 = make_float2(inv_s, inv_s);
+    const float2 big = make_float2(8388608.0f, 8388608.0f);
+    float2 d[4];
+    bool near_tie = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 r = mul2(sub2(make_float2(v[2 * i], v[2 * i + 1]), z2), is2);
+        const float2 t = add2(r, big);
+        d[i] = sub2(r, sub2(t, big));
+        q[2 * i] = __float_as_uint(t.x) - 0x4B000000u;
+        q[2 * i + 1] = __float_as_uint(t.y) - 0x4B000000u;
+        near_tie |= fmaxf(fabsf(d[i].x), fabsf(d[i].y)) > 0.5f - 1.0f / 16384.0f;
+    }
+    if (near_tie) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float di = (i & 1) ? d[i / 2].y : d[i / 2].x;
+            if (fabsf(di) > 0.5f - 1.0f / 16384.0f)
+                q[i] = (uint32_t)rint(((double)v[i] - (double)z) / (double)s);
+        }
+    }
 }
 
 // Lane-held octet of 8 b-bit codes: code i at bits [b*i, b*i+b) of (lo, hi).
@@ -115,11 +166,12 @@ struct Octet {
 
 // GL = lanes per group (g / 8): 4, 8, 16 or 32.
 template <int BITS, int GL>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ packed,
                 uint16_t *__restrict__ scales, uint16_t *__restrict__ zeros, int64_t N, int K) {
     constexpr int group = GL * 8;
     constexpr float qmax = (float)((1 << BITS) - 1);
+    const float rq_lo = __frcp_rd(qmax), rq_hi = __frcp_ru(qmax);
     const int lane = threadIdx.x & 31;
     const int G = K / group;
     const int cpr = (K + kChunk - 1) / kChunk;               // chunks per row
@@ -180,19 +232,36 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
         // divisions); a group is an aligned run of GL lanes, so a shuffle
         // hands it to the others.
         uint32_t sh32 = 0x0400u;
-        if ((lane & (GL - 1)) == 0) sh32 = flat ? flat_scale_bits(mn, z) : scale_bits(mx, z, qmax);
+        if ((lane & (GL - 1)) == 0) sh32 = flat ? flat_scale_bits(mn, z) : scale_bits(mx, z, qmax, rq_lo, rq_hi);
         const uint16_t sh = (uint16_t)__shfl_sync(0xffffffffu, sh32, lane & ~(GL - 1));
         if (k < K) {
             const float s = __half2float(__ushort_as_half(sh));
             const float inv_s = __frcp_rn(s);
             Octet<BITS> o;
             if (!flat) {
+                uint32_t q[8];
+                codes8(cur.v, z, s, inv_s, q);
+                // The mask changes no valid code; it keeps a NaN weight's
+                // code (0, as before) from spilling into its neighbours.
 #pragma unroll
-                for (int i = 0; i < 8; ++i) o.put(i, code_of(cur.v[i], z, s, inv_s, qmax));
+                for (int i = 0; i < 8; ++i) o.put(i, q[i] & ((1u << BITS) - 1u));
             }
             uint8_t *dst = packed + n * row_bytes + (int64_t)(k / 8) * BITS;
+            // b bytes at byte (k / 8) b of the row: one 32-bit store for b = 4,
+            // 16-bit stores for b = 2 and 6 (the row and octet offsets are even),
+            // bytes otherwise.
+            if constexpr (BITS == 4) {
+                *reinterpret_cast<uint32_t *>(dst) = o.lo;
+            } else if constexpr (BITS == 2) {
+                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)o.lo;
+            } else if constexpr (BITS == 6) {
+                reinterpret_cast<uint16_t *>(dst)[0] = (uint16_t)o.lo;
+                reinterpret_cast<uint16_t *>(dst)[1] = (uint16_t)(o.lo >> 16);
+                reinterpret_cast<uint16_t *>(dst)[2] = (uint16_t)o.hi;
+            } else {
 #pragma unroll
-            for (int i = 0; i < BITS; ++i) dst[i] = o.byte(i);
+                for (int i = 0; i < BITS; ++i) dst[i] = o.byte(i);
+            }
             if ((lane & (GL - 1)) == 0) {
                 const int64_t gi = n * G + k / group;
                 scales[gi] = sh;
