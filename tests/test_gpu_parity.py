@@ -263,6 +263,23 @@ def test_qmm_every_bits_full_tiles(bits):
     check_close(y_to_f64(d.run(lb.PATH_QMM)), _oracle_y(L), f"qmm b={bits}")
 
 
+@pytest.mark.parametrize("M,K,N,bits,group", [
+    (128, 128, 130, 4, 128),    # one K step: the second issuing thread has none
+    (40, 384, 300, 3, 128),     # three steps: the two issuing threads take 2 and 1
+    (128, 1920, 500, 5, 128),   # 15 steps over a cluster of 8: CTAs with one or two steps
+    (130, 2304, 250, 2, 256),   # groups spanning two steps, two x tiles, split over a cluster
+    (1, 128, 60, 7, 32),        # g < 128: one issuing thread, four segments per step
+    (40, 640, 300, 6, 64),      # g < 128: five steps of two segments
+])
+def test_qmm_issuers_and_step_counts(M, K, N, bits, group):
+    # With g >= 128 the K steps alternate between two MMA-issuing threads (with
+    # smaller groups one thread issues them all); step counts of one, odd, and
+    # split over a cluster cover every way the steps can fall.
+    L = synth.make_layer(70 + K + bits, M, K, N, bits, group, bias=True, outliers=M > 1)
+    d = DeviceLayer(L)
+    check_close(y_to_f64(d.run(lb.PATH_QMM)), _oracle_y(L), f"qmm {(M, K, N, bits, group)}")
+
+
 @pytest.mark.parametrize("M,name", [(128, "o"), (8, "down"), (128, "gate_up")])
 def test_qmm_split_k_is_deterministic(M, name):
     # Small layers split K over a cluster; the partial sums are added in a
