@@ -394,9 +394,24 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
                 uint32_t h[16];
-                [&]<int... J>(std::integer_sequence<int, J...>) {
-                    ((h[J] = code_pair<BITS, J>(w[blk])), ...);
-                }(std::make_integer_sequence<int, 16>{});
+                if constexpr (BITS == 4) {
+                    // Four pairs per word in nine instructions: even and odd
+                    // nibbles into bytes, bytes into code order, and each
+                    // pair of codes beside the magic byte 0x43.
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t t = w[blk][i] & 0x0F0F0F0Fu, u = (w[blk][i] >> 4) & 0x0F0F0F0Fu;
+                        const uint32_t v0 = ptx::prmt(t, u, 0x5140u), v1 = ptx::prmt(t, u, 0x7362u);
+                        h[4 * i] = ptx::prmt(v0, 0x43434343u, 0x4140u);
+                        h[4 * i + 1] = ptx::prmt(v0, 0x43434343u, 0x4342u);
+                        h[4 * i + 2] = ptx::prmt(v1, 0x43434343u, 0x4140u);
+                        h[4 * i + 3] = ptx::prmt(v1, 0x43434343u, 0x4342u);
+                    }
+                } else {
+                    [&]<int... J>(std::integer_sequence<int, J...>) {
+                        ((h[J] = code_pair<BITS, J>(w[blk])), ...);
+                    }(std::make_integer_sequence<int, 16>{});
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) h[j] = lane == 31 ? 0x3F803F80u : h[j];   // bf16 (1, 1)
                 ptx::tmem_st16(adst + (uint32_t)(blk * 16), h);
@@ -445,15 +460,12 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
             ptx::tc_fence_after();
             bool released = false;                        // one t_empty arrival per warp per segment
 #pragma unroll
-            for (int c2 = 0; c2 < 4; c2 += 2) {          // two chunks per tensor-memory wait
-                uint32_t v[2][16];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int ch = h + 2 * (c2 + u);
-                    if (ch < nchunk) ptx::tmem_ld16(trow + (uint32_t)(b * p.TN + ch * 16), v[u]);
-                }
+            for (int c = 0; c < 4; ++c) {                // one 16-column chunk per tensor-memory wait
+                const int ch = h + 2 * c;
+                uint32_t v[16];
+                if (ch < nchunk) ptx::tmem_ld16(trow + (uint32_t)(b * p.TN + ch * 16), v);
                 ptx::tmem_ld_wait();
-                if (!released && (c2 + 2 >= 4 || h + 2 * (c2 + 2) >= nchunk)) {
+                if (!released && (c + 1 >= 4 || h + 2 * (c + 1) >= nchunk)) {
                     // Last tensor-memory read of this segment: hand the buffer back.
                     ptx::tc_fence_before();
                     __syncwarp();
@@ -462,18 +474,14 @@ qmm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUt
                 }
                 // The group sums X_g of the chunk's columns sit in lane 31 (the
                 // ones row) and are broadcast by shuffles.
+                if (ch < nchunk) {
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int ch = h + 2 * (c2 + u);
-                    if (ch < nchunk) {
-#pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
-                            const float x0 = __shfl_sync(0xFFFFFFFFu, __uint_as_float(v[u][j]), 31);
-                            const float x1 = __shfl_sync(0xFFFFFFFFu, __uint_as_float(v[u][j + 1]), 31);
-                            float2 &a = acc[c2 + u][j / 2];
-                            ptx::ffma2(a, make_float2(__uint_as_float(v[u][j]), __uint_as_float(v[u][j + 1])), s2, a);
-                            ptx::ffma2(a, make_float2(x0, x1), z2, a);
-                        }
+                    for (int j = 0; j < 16; j += 2) {
+                        const float x0 = __shfl_sync(0xFFFFFFFFu, __uint_as_float(v[j]), 31);
+                        const float x1 = __shfl_sync(0xFFFFFFFFu, __uint_as_float(v[j + 1]), 31);
+                        float2 &a = acc[c][j / 2];
+                        ptx::ffma2(a, make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, a);
+                        ptx::ffma2(a, make_float2(x0, x1), z2, a);
                     }
                 }
             }
