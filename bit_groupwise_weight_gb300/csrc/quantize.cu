@@ -164,8 +164,10 @@ struct Octet {
     }
 };
 
-// GL = lanes per group (g / 8): 4, 8, 16 or 32.
-template <int BITS, int GL>
+// GL = lanes per group (g / 8): 4, 8, 16 or 32.  WIDE: the packed matrix is
+// aligned for the 16- and 32-bit stores of b = 2, 4, 6 (it may have any
+// alignment; otherwise every byte is stored on its own).
+template <int BITS, int GL, bool WIDE>
 __global__ void __launch_bounds__(256, 4)
 quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ packed,
                 uint16_t *__restrict__ scales, uint16_t *__restrict__ zeros, int64_t N, int K) {
@@ -248,13 +250,13 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
             }
             uint8_t *dst = packed + n * row_bytes + (int64_t)(k / 8) * BITS;
             // b bytes at byte (k / 8) b of the row: one 32-bit store for b = 4,
-            // 16-bit stores for b = 2 and 6 (the row and octet offsets are even),
-            // bytes otherwise.
-            if constexpr (BITS == 4) {
+            // 16-bit stores for b = 2 and 6 (row and octet offsets are multiples
+            // of 4 and 2 bytes), bytes otherwise or when the matrix is not aligned.
+            if constexpr (WIDE && BITS == 4) {
                 *reinterpret_cast<uint32_t *>(dst) = o.lo;
-            } else if constexpr (BITS == 2) {
+            } else if constexpr (WIDE && BITS == 2) {
                 *reinterpret_cast<uint16_t *>(dst) = (uint16_t)o.lo;
-            } else if constexpr (BITS == 6) {
+            } else if constexpr (WIDE && BITS == 6) {
                 reinterpret_cast<uint16_t *>(dst)[0] = (uint16_t)o.lo;
                 reinterpret_cast<uint16_t *>(dst)[1] = (uint16_t)(o.lo >> 16);
                 reinterpret_cast<uint16_t *>(dst)[2] = (uint16_t)o.hi;
@@ -277,33 +279,45 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
 
 // One resident wave: as many blocks as fit on the device at once (each warp
 // then strides over chunks), or fewer when there are fewer chunks.
-template <int BITS, int GL>
+template <int BITS, int GL, bool WIDE>
 cudaError_t launch_one(const void *w, int dtype, uint8_t *packed, uint16_t *scales,
                        uint16_t *zeros, int64_t N, int K, cudaStream_t stream) {
     int dev = 0, sms = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_kernel<BITS, GL>, 256, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_kernel<BITS, GL, WIDE>, 256, 0);
     if (e != cudaSuccess) return e;
     const int64_t chunks = N * ((K + kChunk - 1) / kChunk);
     const int64_t want = (chunks + 7) / 8;
     const int64_t wave = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
     const unsigned blocks = (unsigned)(want < wave ? want : wave);
-    quantize_kernel<BITS, GL><<<blocks, 256, 0, stream>>>(w, dtype, packed, scales, zeros, N, K);
+    quantize_kernel<BITS, GL, WIDE><<<blocks, 256, 0, stream>>>(w, dtype, packed, scales, zeros, N, K);
     return cudaGetLastError();
+}
+
+template <int BITS, bool WIDE>
+cudaError_t launch_group(const void *w, int dtype, uint8_t *packed, uint16_t *scales,
+                         uint16_t *zeros, int64_t N, int K, int group, cudaStream_t stream) {
+    switch (group) {
+        case 32: return launch_one<BITS, 4, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 64: return launch_one<BITS, 8, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 128: return launch_one<BITS, 16, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 256: return launch_one<BITS, 32, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <int BITS>
 cudaError_t launch_bits(const void *w, int dtype, uint8_t *packed, uint16_t *scales,
                         uint16_t *zeros, int64_t N, int K, int group, cudaStream_t stream) {
-    switch (group) {
-        case 32: return launch_one<BITS, 4>(w, dtype, packed, scales, zeros, N, K, stream);
-        case 64: return launch_one<BITS, 8>(w, dtype, packed, scales, zeros, N, K, stream);
-        case 128: return launch_one<BITS, 16>(w, dtype, packed, scales, zeros, N, K, stream);
-        case 256: return launch_one<BITS, 32>(w, dtype, packed, scales, zeros, N, K, stream);
-        default: return cudaErrorInvalidValue;
+    // Only b = 2, 4, 6 have wide stores; they need 2- or 4-byte alignment.
+    constexpr uintptr_t need = BITS == 4 ? 4 : 2;
+    if constexpr (BITS == 2 || BITS == 4 || BITS == 6) {
+        if ((reinterpret_cast<uintptr_t>(packed) & (need - 1)) == 0)
+            return launch_group<BITS, true>(w, dtype, packed, scales, zeros, N, K, group, stream);
     }
+    return launch_group<BITS, false>(w, dtype, packed, scales, zeros, N, K, group, stream);
 }
 
 }  // namespace

@@ -127,6 +127,25 @@ def test_quantize_special_groups(orc, dtype, bits, group):
     assert np.all(np.abs(w64 - (sf * codes + zf)) <= sf / 2), f"bound {dtype} b={bits} g={group}"
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4, 6])
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_quantize_packed_any_alignment(orc, bits, offset):
+    # The packed output may have any alignment (b = 2, 4, 6 store 16- or
+    # 32-bit words only when it is aligned for them); the bytes must not change.
+    import bit_groupwise_weight_gb300 as lb
+    w32 = synth.make_weights(3, 21, 256, key=(bits, offset))
+    w_dev, w64 = _as_dtype(w32, "bf16")
+    ref, s_ref, z_ref = _gpu_quantize(w_dev, bits, 64)
+    rb = 256 * bits // 8
+    flat = torch.zeros(21 * rb + offset, dtype=torch.uint8, device=w_dev.device)
+    packed = flat[offset:].view(21, rb)
+    assert packed.data_ptr() % 4 != 0 or offset == 0
+    lb.quantize_weights(w_dev, bits, 64, packed)
+    torch.cuda.synchronize()
+    assert np.array_equal(packed.cpu().numpy(), ref), f"b={bits} offset={offset}"
+    assert int(flat[:offset].sum().item()) == 0, "bytes before the output were written"
+
+
 @pytest.mark.parametrize("bits,group", [(3, 64), (4, 128), (7, 32)])
 def test_quantize_full_size_gate_up_sampled(orc, bits, group):
     """Llama 3.1 8B gate+up (K=4096, N=28672) in bf16, checked on sampled rows."""
