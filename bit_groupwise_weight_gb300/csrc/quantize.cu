@@ -17,12 +17,14 @@
 //     1/qmax rounded down, and the same rounded up (every step rounded
 //     outward), so when both bounds round up to the same fp16 that fp16 is
 //     the scale (the fp64 quotient is the fp64 value nearest the exact one,
-//     and no fp32 bound can lie between the two);
+//     and no fp32 bound can lie between the two); when they round to two
+//     adjacent fp16 values, the sign of an exact fp32 residual picks one;
 //   - (w - zero) / scale in fp32 differs from the fp64 quotient by less than
 //     3 * 2^-24 * 2^7 < 2^-15 (it is at most 2^7 and carries three roundings
 //     of 2^-24 relative), so its round-half-even agrees with fp64's unless it
-//     lies within that distance of a half-integer; codes within 2^-14 of one
-//     are recomputed in fp64.
+//     lies within that distance of a half-integer; those codes are decided by
+//     the sign of an exact fp32 residual against that half-integer;
+//   - fp64 itself only where w - zero or max - zero is not exact in fp32.
 // The codes need no clamping: zero <= min and scale >= (max - zero) / qmax,
 // so the exact quotient lies in [0, qmax], and the fp32 and fp64 quotients
 // stay within [0, qmax + 2^-15].
@@ -71,17 +73,22 @@ __device__ __forceinline__ W8 load8(const void *w, int dtype, int64_t k0) {
 }
 
 // fp16 scale: rounded toward +inf of fl64(fl64(mx - z) / qmax).  rq_lo and
-// rq_hi are 1/qmax rounded down and up.  The bounds from the reciprocal are
-// cheap but a little wider than those of directed divisions, which also
-// decide the common case of an exact quotient; fp64 decides the rest.
+// rq_hi are 1/qmax rounded down and up.  When the two bounds round up to
+// different fp16 values lo < hi (adjacent: the bounds are a few fp32 ulps
+// apart), the scale is lo if the quotient is at most lo and hi otherwise.
+// With mx - z exact in fp32, fma(-lo, qmax, mx - z) has the sign of the
+// exact (mx - z) - lo qmax (lo qmax has at most 18 significant bits); a
+// nonzero difference is at least 2^-23 of it, far above the fp64 quotient's
+// rounding, so fp64 lies on the same side of lo.  Otherwise fp64 decides.
 __device__ __forceinline__ uint16_t scale_bits(float mx, float z, float qmax, float rq_lo, float rq_hi) {
     const float d_lo = __fsub_rd(mx, z), d_hi = __fsub_ru(mx, z);
-    uint16_t lo = __half_as_ushort(__float2half_ru(__fmul_rd(d_lo, rq_lo)));
-    uint16_t hi = __half_as_ushort(__float2half_ru(__fmul_ru(d_hi, rq_hi)));
+    const uint16_t lo = __half_as_ushort(__float2half_ru(__fmul_rd(d_lo, rq_lo)));
+    const uint16_t hi = __half_as_ushort(__float2half_ru(__fmul_ru(d_hi, rq_hi)));
     if (lo == hi) return lo;
-    lo = __half_as_ushort(__float2half_ru(__fdiv_rd(d_lo, qmax)));
-    hi = __half_as_ushort(__float2half_ru(__fdiv_ru(d_hi, qmax)));
-    if (lo == hi) return lo;
+    if (d_lo == d_hi && hi == lo + 1u) {
+        const float res = fmaf(-__half2float(__ushort_as_half(lo)), qmax, d_lo);
+        return res <= 0.0f ? lo : hi;
+    }
     const double t = ((double)mx - (double)z) / (double)qmax;
     // Directed rounding to fp16 through fp32 in the same direction equals
     // directed rounding to fp16 directly: every fp16 is an fp32.
@@ -117,6 +124,26 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     return *reinterpret_cast<float2 *>(&r);
 }
 
+// Code of a weight whose fp32 quotient r lies within 2^-14 of the half-integer
+// h = rint(r) + 1/2 sign(r - rint(r)); the fp64 quotient is then h - 1/2 or
+// h + 1/2 after rounding.  When v - z is exact in fp32 (its downward and
+// upward roundings agree), fma(-h, s, v - z) has the sign of the exact
+// (v - z) - h s: h s has at most 19 significant bits, so the fma rounds once.
+// A nonzero residual is at least 2^-23 h s (its last bit is that of v - z or
+// of h s), far above the fp64 quotient's rounding, so fp64 rounds to the
+// same side; a zero residual is an exact tie, which fp64 rounds to even.
+// Otherwise fp64 decides.
+__device__ __noinline__ uint32_t code_near_tie(float v, float z, float s, uint32_t q, float d) {
+    const float lo = __fsub_rd(v, z), hi = __fsub_ru(v, z);
+    if (lo != hi) return (uint32_t)rint(((double)v - (double)z) / (double)s);
+    const float h = d > 0.0f ? (float)q + 0.5f : (float)q - 0.5f;
+    const float res = fmaf(-h, s, lo);
+    const uint32_t below = (uint32_t)(h - 0.5f);
+    if (res > 0.0f) return below + 1u;
+    if (res < 0.0f) return below;
+    return below + (below & 1u);                      // exact tie: to even
+}
+
 // Codes of a lane's 8 weights: rint(fl64(fl64(v - z) / s)) (see the header).
 // r = (v - z) * (1/s) in fp32; t = r + 2^23 rounds r to the nearest integer,
 // ties to even, into t's low mantissa bits (0 <= r < 2^22), so t's bits are
@@ -140,8 +167,7 @@ __device__ __forceinline__ void codes8(const float (&v)[8], float z, float s, fl
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float di = (i & 1) ? d[i / 2].y : d[i / 2].x;
-            if (fabsf(di) > 0.5f - 1.0f / 16384.0f)
-                q[i] = (uint32_t)rint(((double)v[i] - (double)z) / (double)s);
+            if (fabsf(di) > 0.5f - 1.0f / 16384.0f) q[i] = code_near_tie(v[i], z, s, q[i], di);
         }
     }
 }
