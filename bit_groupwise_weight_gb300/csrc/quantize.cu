@@ -32,31 +32,35 @@
 // bullet 2).
 //
 // Work unit: one warp per chunk of 256 consecutive weights of a row.  Lane l
-// loads weights [8l, 8l+8) with 16-byte loads; a group of g weights spans g/8
-// lanes, whose min/max is a segmented shuffle reduction; the lane's 8 codes
-// are one octet, written as b bytes at byte l*b of the chunk's packed bytes.
+// takes weights [8l, 8l+8); a group of g weights spans g/8 lanes, whose
+// min/max is a segmented shuffle reduction; the lane's 8 codes are one octet,
+// written as b bytes at byte l*b of the chunk's packed bytes.  The weights
+// arrive through a per-warp ring of 8 chunks in shared memory, filled with
+// 16-byte asynchronous copies (cp.async) 7 chunks ahead of the one being
+// coded, so that each warp keeps several KB of loads in flight.
 #include "common.cuh"
 
 namespace lowbit {
 namespace {
 
 constexpr int kChunk = 256;          // weights per warp per step
+constexpr int kRing = 8;             // chunks of a warp in flight (shared-memory ring)
+constexpr int kWarps = 8;            // warps per block
 
 struct W8 {
     float v[8];
 };
 
-// Weights [k0, k0+8) of the flat input, converted exactly to fp32.
-__device__ __forceinline__ W8 load8(const void *w, int dtype, int64_t k0) {
+// A lane's 8 weights from their raw bytes (16 for 16-bit inputs, 32 for
+// fp32), converted exactly to fp32.
+__device__ __forceinline__ W8 convert8(int dtype, uint4 u, uint4 u2) {
     W8 r;
     if (dtype == LOWBIT_DTYPE_F32) {
-        const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(w) + k0);
-        const float4 a = __ldcs(p), b = __ldcs(p + 1);
-        r.v[0] = a.x; r.v[1] = a.y; r.v[2] = a.z; r.v[3] = a.w;
-        r.v[4] = b.x; r.v[5] = b.y; r.v[6] = b.z; r.v[7] = b.w;
+        r.v[0] = __uint_as_float(u.x); r.v[1] = __uint_as_float(u.y);
+        r.v[2] = __uint_as_float(u.z); r.v[3] = __uint_as_float(u.w);
+        r.v[4] = __uint_as_float(u2.x); r.v[5] = __uint_as_float(u2.y);
+        r.v[6] = __uint_as_float(u2.z); r.v[7] = __uint_as_float(u2.w);
     } else {
-        const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(
-            reinterpret_cast<const uint16_t *>(w) + k0));
         const uint32_t words[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -71,6 +75,15 @@ __device__ __forceinline__ W8 load8(const void *w, int dtype, int64_t k0) {
     }
     return r;
 }
+
+// 16-byte asynchronous copy global -> shared (L2 only); src_bytes 0 fills zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 
 // fp16 scale: rounded toward +inf of fl64(fl64(mx - z) / qmax).  rq_lo and
 // rq_hi are 1/qmax rounded down and up.  When the two bounds round up to
@@ -194,7 +207,7 @@ struct Octet {
 // aligned for the 16- and 32-bit stores of b = 2, 4, 6 (it may have any
 // alignment; otherwise every byte is stored on its own).
 template <int BITS, int GL, bool WIDE>
-__global__ void __launch_bounds__(256, 4)
+__global__ void __launch_bounds__(256, 3)
 quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ packed,
                 uint16_t *__restrict__ scales, uint16_t *__restrict__ zeros, int64_t N, int K) {
     constexpr int group = GL * 8;
@@ -207,7 +220,14 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
     const int64_t row_bytes = (int64_t)K * BITS / 8;
 
-    int64_t c = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    // The warp's ring: kRing slots of 32 lanes x 32 bytes (16-bit inputs use
+    // the first 16 bytes of a lane's 32).
+    __shared__ __align__(16) uint8_t ring[kWarps][kRing][32 * 32];
+    const int wib = threadIdx.x >> 5;
+    const uint32_t ring0 = (uint32_t)__cvta_generic_to_shared(&ring[wib][0][lane * 32]);
+    const int esz = dtype == LOWBIT_DTYPE_F32 ? 4 : 2;
+
+    int64_t c = (int64_t)blockIdx.x * (blockDim.x / 32) + wib;
     if (c >= chunks) return;                                 // whole warp leaves together
     // Chunk c is row c / cpr, chunk c % cpr of the row; the warp strides by
     // `warps` chunks, i.e. dn rows and dc chunks with a carry.
@@ -216,16 +236,40 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
     int64_t n = c / cpr;
     int kc = (int)(c - n * cpr);
     int k = kc * kChunk + lane * 8;
-    W8 cur{};
-    if (k < K) cur = load8(w, dtype, n * K + k);
+    // Prefetch cursor: kRing - 1 chunks ahead of (c, n, kc), each copy group
+    // committed whether or not it copies anything, so that waiting for all but
+    // the newest kRing - 1 groups always means "this chunk has landed".
+    int64_t cp_c = c, cp_n = n;
+    int cp_kc = kc;
+    auto issue = [&](int slot) {
+        const int kk = cp_kc * kChunk + lane * 8;
+        if (cp_c < chunks) {
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(w) + (cp_n * K + kk) * esz;
+            const uint32_t nb = kk < K ? 16u : 0u;
+            const uint32_t dst = ring0 + (uint32_t)(slot * 32 * 32);
+            cp_async16(dst, kk < K ? src : w, nb);
+            if (esz == 4) cp_async16(dst + 16, kk < K ? src + 16 : w, nb);
+        }
+        cp_async_commit();
+        cp_c += warps;
+        cp_n += dn;
+        cp_kc += dc;
+        if (cp_kc >= cpr) { cp_kc -= cpr; ++cp_n; }
+    };
+#pragma unroll
+    for (int j = 0; j < kRing - 1; ++j) issue(j);
+    int slot = 0;                                        // ring slot of this chunk
     for (; c < chunks; c += warps) {
-        // Register double buffer: the next chunk's weights load while this one is coded.
+        issue(slot == 0 ? kRing - 1 : slot - 1);         // into the slot read last iteration
+        cp_async_wait<kRing - 1>();                      // this chunk's copies have landed
+        const uint8_t *mine = &ring[wib][slot][lane * 32];
+        if (++slot == kRing) slot = 0;
+        const W8 cur = convert8(dtype, *reinterpret_cast<const uint4 *>(mine),
+                                *reinterpret_cast<const uint4 *>(mine + 16));
         int64_t n2 = n + dn;
         int kc2 = kc + dc;
         if (kc2 >= cpr) { kc2 -= cpr; ++n2; }
         const int k2 = kc2 * kChunk + lane * 8;
-        W8 nxt{};
-        if (c + warps < chunks && k2 < K) nxt = load8(w, dtype, n2 * K + k2);
         // A group lies wholly inside or wholly outside the row (K % group == 0),
         // so lanes past the row end only ever reduce among themselves.
         float mn = cur.v[0], mx = cur.v[0];
@@ -296,7 +340,6 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
                 zeros[gi] = zh;
             }
         }
-        cur = nxt;
         n = n2;
         kc = kc2;
         k = k2;
@@ -318,7 +361,7 @@ cudaError_t launch_one(const void *w, int dtype, uint8_t *packed, uint16_t *scal
     const int64_t want = (chunks + 7) / 8;
     const int64_t wave = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
     const unsigned blocks = (unsigned)(want < wave ? want : wave);
-    quantize_kernel<BITS, GL, WIDE><<<blocks, 256, 0, stream>>>(w, dtype, packed, scales, zeros, N, K);
+    quantize_kernel<BITS, GL, WIDE><<<blocks, kWarps * 32, 0, stream>>>(w, dtype, packed, scales, zeros, N, K);
     return cudaGetLastError();
 }
 
