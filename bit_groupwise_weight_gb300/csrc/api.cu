@@ -92,16 +92,17 @@ lowbit_status check_linear_args(const uint16_t *x, const uint8_t *w, const uint1
 // (qmm), measured on GB300 for the Llama-3.1-8B shapes at b = 4, g = 128,
 // M = 2..32.  The tensor-core decode kernel reads the weights once per launch
 // of up to 2 (g = 32), 4 (g = 64) or 8 (g >= 128) rows of x; qmm's time is
-// nearly flat in M up to 32.  One decode launch beat qmm on every shape (down
-// at M = 8: 31.7 vs 32.8 us); two launches beat it only for the widest layer
-// (gate+up, N = 28672: 50 vs 66 us at M = 16; qkv, o and down lost).  Where
-// the decode kernel does not take the shape, the CUDA-core kernel reads the
-// weights once per two rows of x and wins up to M = 2, or up to M = 6 for
-// layers of N >= 9424 outputs.
+// nearly flat in M up to 32.  One decode launch beat qmm on every shape but
+// down (K = 14336, split over 4-CTA clusters) at M = 8: 29.5 vs 24.2 us (at
+// M = 4: 19.6 vs 24.1); two launches lost everywhere (gate+up at M = 16: 50.1
+// vs 47.2 us).  Where the decode kernel does not take the shape, the CUDA-core
+// kernel reads the weights once per two rows of x and wins up to M = 2, or up
+// to M = 6 for layers of N >= 9424 outputs.
 constexpr int64_t kQmvMaxM = 2;
 constexpr int64_t kQmvMaxMWide = 6;
 constexpr int64_t kWideN = 9424;          // 76 row tiles of 124: half the SMs
-constexpr int64_t kTwoPassN = 20000;      // two decode launches still beat qmm
+constexpr int64_t kClusterK = 8192;       // above: the decode kernel splits K over >= 3 CTAs
+constexpr int64_t kClusterMaxM = 4;       // ... and loses to qmm beyond this many rows
 
 }  // namespace
 
@@ -167,7 +168,7 @@ lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int gr
     if (lowbit::qmv_mma_shape_ok(K, group)) {
         const int64_t rows = lowbit::qmv_mma_rows(group);
         const int64_t passes = (M + rows - 1) / rows;
-        return (passes <= 1 || (passes == 2 && N >= kTwoPassN)) ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
+        return (passes <= 1 && !(K > kClusterK && M > kClusterMaxM)) ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
     }
     return (M <= kQmvMaxM || (M <= kQmvMaxMWide && N >= kWideN)) ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
 }

@@ -215,8 +215,8 @@ LOWBIT_API lowbit_status lowbit_linear_swiglu(const uint16_t *x, const uint8_t *
  * GB300: LOWBIT_PATH_QMV when the tensor-core decode kernel covers M in one
  * launch (K a multiple of 256 up to 32768 with K/group a multiple of 8:
  * M <= 2 for group 32, M <= 4 for group 64, M <= 8 for groups 128 and 256),
- * or in two launches for layers of N >= 20000 outputs; for other K, M <= 2,
- * or M <= 6 when N >= 9424; and whenever K is not a multiple of 128.
+ * except M > 4 with K > 8192; for other K, M <= 2, or M <= 6 when
+ * N >= 9424; and whenever K is not a multiple of 128.
  * LOWBIT_PATH_QMM otherwise.  The choice assumes x, the packed weights,
  * scales and zeros 16-byte aligned (the decode path still runs, slower,
  * when they are not).

@@ -69,16 +69,19 @@ def test_select_path(lib):
     assert lb.select_path(0, 4096, 4096, 4, 64) == lb.PATH_QMV
     assert lb.select_path(128, 4096, 4096, 4, 64) == lb.PATH_QMM
     # Measured crossovers.  The tensor-core decode kernel takes 2 / 4 / 8 rows of x
-    # per launch for g = 32 / 64 / >= 128: one launch always, two only when N >= 20000.
+    # per launch for g = 32 / 64 / >= 128: one launch, except above 4 rows when
+    # K > 8192 (split over clusters of three or more CTAs); never two.
     assert lb.select_path(4, 4096, 4096, 4, 64) == lb.PATH_QMV
     assert lb.select_path(5, 4096, 4096, 4, 64) == lb.PATH_QMM
     assert lb.select_path(8, 4096, 6144, 4, 128) == lb.PATH_QMV
     assert lb.select_path(9, 4096, 6144, 4, 128) == lb.PATH_QMM
-    assert lb.select_path(8, 14336, 4096, 7, 256) == lb.PATH_QMV
+    assert lb.select_path(4, 14336, 4096, 7, 256) == lb.PATH_QMV
+    assert lb.select_path(5, 14336, 4096, 7, 256) == lb.PATH_QMM
+    assert lb.select_path(8, 8192, 3072, 4, 128) == lb.PATH_QMV
     assert lb.select_path(2, 4096, 4096, 4, 32) == lb.PATH_QMV
     assert lb.select_path(3, 4096, 4096, 4, 32) == lb.PATH_QMM
-    assert lb.select_path(16, 4096, 28672, 4, 128) == lb.PATH_QMV
-    assert lb.select_path(17, 4096, 28672, 4, 128) == lb.PATH_QMM
+    assert lb.select_path(8, 4096, 28672, 4, 128) == lb.PATH_QMV
+    assert lb.select_path(9, 4096, 28672, 4, 128) == lb.PATH_QMM
     assert lb.select_path(16, 4096, 16384, 4, 128) == lb.PATH_QMM
     # Shapes the decode kernel does not take: the CUDA-core kernel's crossover
     # (K % 256 != 0; K / group not a multiple of 8).
