@@ -28,19 +28,20 @@
 // unpacked codes never travel through shared memory (neither as stores nor as
 // MMA operand reads), which leaves shared-memory bandwidth to the x tiles.
 //
-// Warp roles (448 threads):
+// Warp roles (480 threads):
 //   warp 0       TMA producers: lane 0 streams the 128 x 16b packed-code
 //                tiles (one 2D tensor copy per stage) into a deep ring that
 //                the unpackers free; lane 1 streams the x tiles (two 2D copies,
 //                64-wide, 128-byte swizzle) into a ring that MMA completion
 //                frees;
-//   warp 1       allocates tensor memory; one lane issues the MMAs
-//                (tcgen05.mma kind::f16, A from tensor memory, bf16 x bf16 ->
-//                fp32) and commits them to mbarriers that free buffers or hand
-//                a segment on;
-//   warps 2..5   unpack: one thread per tile row (its TMEM lane) turns the
+//   warps 1, 2   lane 0 of each issues the MMAs (tcgen05.mma kind::f16, A from
+//                tensor memory, bf16 x bf16 -> fp32) of alternate K steps when
+//                a segment is one step long (one issuer otherwise) and commits
+//                them to mbarriers that free buffers or hand a segment on;
+//                warp 1 also allocates and frees tensor memory;
+//   warps 3..6   unpack: one thread per tile row (its TMEM lane) turns the
 //                row's codes into bf16 pairs and writes them with tcgen05.st;
-//   warps 6..13  accumulate: per segment read P_g and X_g from tensor memory,
+//   warps 7..14  accumulate: per segment read P_g and X_g from tensor memory,
 //                apply scale and zero in fp32, and at the end add the bias and
 //                store y (two warps per tensor-memory lane quarter).
 // All waits are bounded (about one second) and count a timeout instead of
