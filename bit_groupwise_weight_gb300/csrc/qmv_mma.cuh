@@ -38,9 +38,9 @@
 // scale/zero epilogue runs once per slice and row tile.
 //
 // CTA = W consumer warps (K/ks = 256 W, W <= 16), one producer warp and one
-// finishing warp.  The producer copies each staged row's K range with a
-// one-dimensional TMA bulk copy into a padded ring of shared-memory stages
-// (mbarrier completion).  Consumers reduce a tile's partial sums over the
+// finishing warp.  The producer copies each 16-row tile with 2D TMA tensor
+// copies (one box per part of the CTA's K range, as wide as the part plus its
+// row padding) into a ring of shared-memory stages (mbarrier completion).  Consumers reduce a tile's partial sums over the
 // four lanes of a row group with shuffles and store them, per warp, into a
 // reduction buffer of the cluster's first CTA (DSMEM); its finishing warp
 // adds the ks * W partials of every output in a fixed order, adds the bias,
@@ -242,6 +242,14 @@ __device__ __forceinline__ uint32_t code_pair(const uint32_t (&w)[B]) {
     }
 }
 
+// Pair K of the plan as the fp16 pair (2^plo, 2^phi): against B = x' 2^-p in
+// the same k-slots the tensor cores return sum x' (the codes' positions undone).
+template <int B, int K>
+constexpr uint32_t pos_pair() {
+    constexpr PairSpec s = kPlan<B>.pr[K];
+    return ((uint32_t)(15 + s.hi_p) << 26) | ((uint32_t)(15 + s.lo_p) << 10);
+}
+
 // ---------------------------------------------------------------------------
 // Launch parameters.
 // ---------------------------------------------------------------------------
@@ -319,9 +327,8 @@ __device__ __forceinline__ int64_t tile_row0(const Params &p, int lt) {
     return p.F == 0 ? (int64_t)lt * kTile : (int64_t)((lt & 1) ? p.F : 0) + (int64_t)(lt >> 1) * kTile;
 }
 
-// 8 bf16 of x (16-byte aligned) as fp32.
-__device__ __forceinline__ void load_x8(const uint16_t *p, float (&v)[8]) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+// 8 bf16 of x (one 16-byte load) as fp32.
+__device__ __forceinline__ void x8_to_float(const uint4 &u, float (&v)[8]) {
     const uint32_t a[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -359,6 +366,23 @@ __device__ __forceinline__ void tile_block(uint32_t rowa, uint32_t rowb, const u
             constexpr int c = 8 * BETA + C;
             if constexpr ((DB2 ? BETA : (C & 1)) == 0) ptx::mma_16816_f16(d0, a0, a1, a2, a3, bq[c][0], bq[c][1]);
             else ptx::mma_16816_f16(d1, a0, a1, a2, a3, bq[c][0], bq[c][1]);
+        }(), ...);
+    }(std::make_integer_sequence<int, 8>{});
+}
+
+// The group sums of every B column with the B fragments alone: A rows 0..7
+// hold 2^p per k-slot (D = X = sum x'), rows 8..15 hold 1024 (D = O = sum
+// 1024 2^-p x', the offset P' carries).  Thread (gid, t) thus receives X and
+// O of exactly its accumulator columns 2t, 2t + 1, in the same column sets
+// as tile_block's d0 / d1.
+template <int BITS, bool DB2, int BETA>
+__device__ __forceinline__ void group_sums(const uint32_t (&bq)[16][2], float (&d0)[4], float (&d1)[4]) {
+    [&]<int... C>(std::integer_sequence<int, C...>) {
+        ((void)[&] {
+            constexpr uint32_t a0 = pos_pair<BITS, 2 * C>(), a2 = pos_pair<BITS, 2 * C + 1>();
+            constexpr int c = 8 * BETA + C;
+            if constexpr ((DB2 ? BETA : (C & 1)) == 0) ptx::mma_16816_f16(d0, a0, kMagic, a2, kMagic, bq[c][0], bq[c][1]);
+            else ptx::mma_16816_f16(d1, a0, kMagic, a2, kMagic, bq[c][0], bq[c][1]);
         }(), ...);
     }(std::make_integer_sequence<int, 8>{});
 }
@@ -525,7 +549,6 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
         const int gpb = max(1, 128 >> p.log2g);               // groups per 128-code half
         const int gpc = DB2 ? gpb : gsl;                      // groups per column set
         const int gw0 = kw0 >> p.log2g;                       // first group of the slice
-        const int lpg = min(32, (1 << p.log2g) >> 3);         // lanes per group (8 codes a lane)
         const int mcol = gid % MP, jcol = gid / MP;           // this thread's B column
         const bool bvalid = mcol < M && jcol < gpc;
 
@@ -533,7 +556,6 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
         // j = (2t + e) / MP of each column set.  Unused columns read the
         // slice's first groups (finite data) and add zero.
         int gk[NB][2];
-        bool cvalid[NB][2];
         int me[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -542,8 +564,7 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
 #pragma unroll
             for (int bb = 0; bb < NB; ++bb) {
                 const int j = col / MP;
-                cvalid[bb][e] = me[e] < M && j < gpc;
-                gk[bb][e] = gw0 + (cvalid[bb][e] ? bb * gpb + j : 0);
+                gk[bb][e] = gw0 + ((me[e] < M && j < gpc) ? bb * gpb + j : 0);
             }
         }
         // MP == 1: columns 2t, 2t + 1 are adjacent groups (both used or both
@@ -552,17 +573,14 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
         const int gbase = rank * p.gcta;                      // first group of a staged scale row
         const int gpair = gw0 - gbase + ((MP == 1 && 2 * t < gsl) ? 2 * t : 0);
 
-        // Per x row: the scale 2^e, and the group sums X and O of this thread's columns.
-        // Per x row m: the scale 2^e of the warp's slice, the group sums X and O
-        // of this thread's columns, and the B fragments of the threads whose
-        // column holds row m.  Lane l converts the slice's codes [8l, 8l + 8)
-        // (block l / 16 of lane quarter (l / 4) % 4) and writes them, in
-        // fragment order, to the warp's table; a thread reads its 64 fp16
-        // values back as 32 words and keeps the blocks of its column group.
+        // Per x row m: the scale 2^e of the warp's slice and the B fragments of
+        // the threads whose column holds row m.  Lane l converts the slice's
+        // codes [8l, 8l + 8) (block l / 16 of lane quarter (l / 4) % 4) and
+        // writes them, in fragment order, to the warp's table; a thread reads
+        // its 64 fp16 values back as 32 words and keeps the blocks of its
+        // column group.  The group sums X and O follow from the fragments on
+        // the tensor cores (group_sums).
         float isc[2] = {1.f, 1.f};
-        float X[NB][2], O[NB][2];
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb) X[bb][0] = X[bb][1] = O[bb][0] = O[bb][1] = 0.f;
         uint32_t bq[16][2];
         uint8_t *scr = smem + p.scr_off + (size_t)warp * kScrBytes;
         const int lw = lane & 3;                               // which 8 codes of the lane's block
@@ -571,50 +589,40 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
         const uint32_t poss = lw == 0 ? code_pos<BITS>(0) : lw == 1 ? code_pos<BITS>(1)
                             : lw == 2 ? code_pos<BITS>(2) : code_pos<BITS>(3);
         uint16_t *srow = reinterpret_cast<uint16_t *>(scr + ((lane >> 2) & 3) * kScrRow) + 32 * (lane >> 4);
+        // x rows come through a queue of up to four loads in flight (one load
+        // latency for M <= 4 instead of M); row m is always xr[0].
+        constexpr int kQ = MP < 4 ? MP : 4;
+        const uint16_t *xlane = p.x + kw0 + 8 * lane;
+        uint4 xr[kQ];
+#pragma unroll
+        for (int m = 0; m < kQ; ++m)
+            xr[m] = m < M ? __ldg(reinterpret_cast<const uint4 *>(xlane + (int64_t)m * p.K)) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
         for (int m = 0; m < MP; ++m) {
             float xv[8];
-            if (m < M) load_x8(p.x + (int64_t)m * p.K + kw0 + 8 * lane, xv);
-            else
+            x8_to_float(xr[0], xv);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) xv[i] = 0.f;
+            for (int j = 0; j + 1 < kQ; ++j) xr[j] = xr[j + 1];
+            if constexpr (MP > kQ)
+                xr[kQ - 1] = m + kQ < M ? __ldg(reinterpret_cast<const uint4 *>(xlane + (int64_t)(m + kQ) * p.K))
+                                        : make_uint4(0u, 0u, 0u, 0u);
             float mx = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(xv[i]));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            // A non-negative float's bits order like its value: one warp-wide
+            // integer maximum.
+            mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
             int ex = 0;
             if (mx > 0.f) {
                 (void)frexpf(mx, &ex);                   // mx = f 2^ex, f in [0.5, 1)
                 ex = min(126, max(-126, 15 - ex));       // mx 2^ex in [2^14, 2^15)
             }
             const float sc = pow2f(ex);
-            float xs = 0.f, os = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int pp = (int)((poss >> (4 * i)) & 15u);
-                const float v = xv[i] * sc;
-                const __half h = __float2half_rn(v * pow2f(-pp));
-                xs += v;
-                os += 1024.f * __half2float(h);
-                srow[(slots >> (8 * i)) & 255u] = __half_as_ushort(h);
+                srow[(slots >> (8 * i)) & 255u] = __half_as_ushort(__float2half_rn(xv[i] * sc * pow2f(-pp)));
             }
-            for (int o = 1; o < lpg; o <<= 1) {
-                xs += __shfl_xor_sync(0xffffffffu, xs, o);
-                os += __shfl_xor_sync(0xffffffffu, os, o);
-            }
-#pragma unroll
-            for (int bb = 0; bb < NB; ++bb)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int src = (gk[bb][e] - gw0) * lpg;
-                    const float xg = __shfl_sync(0xffffffffu, xs, src & 31);
-                    const float og = __shfl_sync(0xffffffffu, os, src & 31);
-                    if (cvalid[bb][e] && me[e] == m) {
-                        X[bb][e] = xg;
-                        O[bb][e] = og;
-                    }
-                }
             if (m == me[0]) isc[0] = pow2f(-ex);
             if (m == me[1]) isc[1] = pow2f(-ex);
             __syncwarp();
@@ -638,6 +646,26 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
             for (int c = 0; c < 8; ++c) {
                 bq[8 * beta + c][0] = keep ? bq[8 * beta + c][0] : 0u;
                 bq[8 * beta + c][1] = keep ? bq[8 * beta + c][1] : 0u;
+            }
+        }
+        // X and O of this thread's columns (zero for unused columns, whose B
+        // fragments are zero).
+        float X[NB][2], O[NB][2];
+        {
+            float g0[4] = {0.f, 0.f, 0.f, 0.f}, g1[4] = {0.f, 0.f, 0.f, 0.f};
+            group_sums<BITS, DB2, 0>(bq, g0, g1);
+            group_sums<BITS, DB2, 1>(bq, g0, g1);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                if constexpr (DB2) {
+                    X[0][e] = g0[e];
+                    O[0][e] = g0[2 + e];
+                    X[NB - 1][e] = g1[e];
+                    O[NB - 1][e] = g1[2 + e];
+                } else {
+                    X[0][e] = g0[e] + g1[e];
+                    O[0][e] = g0[2 + e] + g1[2 + e];
+                }
             }
         }
 
