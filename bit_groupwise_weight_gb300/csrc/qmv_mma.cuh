@@ -402,6 +402,63 @@ __device__ __forceinline__ float sum_partials(const float *red, int nsrc, int st
     return ((c[0] + c[1]) + (c[2] + c[3])) + ((c[4] + c[5]) + (c[6] + c[7]));
 }
 
+// The outputs of one reduction stage (tiles lta .. lta + nts - 1), summed over
+// their nsrc partials by threads th = 0 .. nth - 1 (nth a multiple of 32), add
+// the bias, round once to bf16 and store y.  When threads outnumber outputs,
+// Q = 2, 4 or 8 neighbouring lanes share an output: lane q of the group adds
+// partials q, q + Q, ... and a butterfly combines the group.  Every warp runs
+// the same number of passes (the shuffles need whole warps); the order of the
+// additions is fixed, so results are the same on every call.
+template <int MP>
+__device__ __forceinline__ void finish_stage(const Params &p, const float *red, int lta, int nts, int nsrc,
+                                             int th, int nth) {
+    const int step = p.RS * kTile * MP;                       // floats between two sources' partials
+    const bool gated = p.F != 0;
+    const int nout = (gated ? nts / 2 : nts) * kTile * MP;
+    int Q = 1;
+    while (Q < 8 && 2 * Q <= nsrc && 2 * Q * nout <= nth) Q *= 2;
+    const int lane = th & 31, q = lane & (Q - 1);
+    auto psum = [&](const float *a0) {
+        float a;
+        if (Q == 1) {
+            a = sum_partials(a0, nsrc, step);
+        } else {
+            a = 0.f;
+            for (int src = q; src < nsrc; src += Q) a += a0[src * step];
+            for (int o = 1; o < Q; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        }
+        return a;
+    };
+    for (int ob = (th >> 5) * (32 / Q); ob < nout; ob += nth / Q) {
+        const int o = ob + lane / Q;
+        const bool valid = o < nout && q == 0;
+        const int oo = o < nout ? o : 0;
+        const int rr = oo / MP, m = oo % MP;
+        if (!gated) {
+            const int row = (lta + rr / kTile) * kTile + rr % kTile;
+            float a = psum(red + rr * MP + m);
+            if (valid && m < p.M && row < p.N) {
+                if (p.bias != nullptr) a += half_bits_to_float(p.bias[row]);
+                p.y[(int64_t)m * p.N + row] = float_to_bf16_bits(a);
+            }
+        } else {
+            // Tile 2i of the stage is a gate tile, 2i + 1 its up tile.
+            const int ip = rr / kTile, r = rr % kTile;
+            const int f = ((lta >> 1) + ip) * kTile + r;
+            const int ra = (2 * ip) * kTile + r, ru = ra + kTile;
+            float a = psum(red + ra * MP + m);
+            float u = psum(red + ru * MP + m);
+            if (valid && m < p.M && f < p.F) {
+                if (p.bias != nullptr) {
+                    a += half_bits_to_float(p.bias[f]);
+                    u += half_bits_to_float(p.bias[p.F + f]);
+                }
+                p.y[(int64_t)m * p.F + f] = float_to_bf16_bits(silu_mul(a, u));
+            }
+        }
+    }
+}
+
 // Bounded waits and arrivals on the reduction barriers: cluster scope when
 // the K range is split over a cluster, CTA scope (no fence) otherwise.
 __device__ __forceinline__ bool red_wait(bool cluster, uint32_t bar, uint32_t parity) {
@@ -435,6 +492,12 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
     const int lt0 = u0 * p.unit;
     const int ntl = max(0, min(nu * p.unit, p.tiles - lt0));    // this cluster's tiles
     const int nst = (ntl + p.RS - 1) / p.RS;                      // and stages
+    // With M >= 4 rows of x a stage has 64+ outputs per tile, and the
+    // finishing warp's last stage (cold code, once per call) was the call's
+    // tail: there the consumers finish the last stage together when a call has
+    // at most two stages (o at M = 8: 7.9 -> 6.9 us).  With more stages the
+    // finishing warp's code is warm by the last one and it stays faster.
+    const bool consumers_finish = MP >= 4 && nst >= 1 && nst <= 2;
 
     ptx::pdl_launch_dependents();
     if (tid == 0) {
@@ -493,13 +556,14 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
         for (int i = max(0, s - p.NS); i < s; ++i)
             if (!ptx::mbar_wait(full0 + 8 * (i % p.NS), (i / p.NS) & 1, &g_mma_timeouts)) break;
     } else if (warp == W + 1) {
-        // ---------------- finisher (first CTA of the cluster): sum the partials.
+        // ---------------- finisher (first CTA of the cluster): sum the partials
+        // of every stage (but the last when the consumers finish it).
         ptx::pdl_wait();            // y and bias: only after the previous kernel in the stream
         if (rank == 0) {
             const int nsrc = ks * W;
             const int rows_stage = p.RS * kTile;
             bool ok = true;
-            for (int s = 0; s < nst; ++s) {
+            for (int s = 0; s + (consumers_finish ? 1 : 0) < nst; ++s) {
                 const int buf = s % kRedBufs;
                 if (ok) ok = red_wait(clustered, rfull0 + 8 * buf, (s / kRedBufs) & 1);
                 const int lta = lt0 + s * p.RS;
@@ -800,6 +864,22 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
                 stage = sb + p.ring_off;
                 fpar ^= 1u;
             }
+        }
+        // The last stage, when the consumers finish it: the first CTA's
+        // consumers meet at a named barrier (the CTA's own partials are then
+        // written, and no warp polls while others still compute), await a
+        // cluster's other CTAs on the stage's barrier, and sum the stage's
+        // outputs together.  No stage follows, so its buffer is not handed
+        // back.
+        if (consumers_finish && rank == 0) {
+            const int s = nst - 1, buf = s % kRedBufs;
+            ptx::named_sync(1, (uint32_t)W * 32u);
+            if (ok && clustered) ok = red_wait(true, rfull0 + 8 * buf, (s / kRedBufs) & 1);
+            ok = __all_sync(0xffffffffu, ok);
+            const int lta = lt0 + s * p.RS;
+            const int nts = min(p.RS, lt0 + ntl - lta);
+            const float *red = reinterpret_cast<const float *>(smem + p.red_off) + (size_t)buf * p.red_floats;
+            if (ok) finish_stage<MP>(p, red, lta, nts, ks * W, warp * 32 + lane, W * 32);
         }
     }
     if (clustered) ptx::cluster_sync();
