@@ -89,20 +89,37 @@ lowbit_status check_linear_args(const uint16_t *x, const uint8_t *w, const uint1
 }
 
 // Crossover between the decode kernels and the batched tensor-core kernel
-// (qmm), measured on GB300 for the Llama-3.1-8B shapes at b = 4, g = 128,
-// M = 2..32.  The tensor-core decode kernel reads the weights once per launch
-// of up to 2 (g = 32), 4 (g = 64) or 8 (g >= 128) rows of x; qmm's time is
-// nearly flat in M up to 32.  One decode launch beat qmm on every shape but
-// down (K = 14336, split over 4-CTA clusters) at M = 8: 29.5 vs 24.2 us (at
-// M = 4: 19.6 vs 24.1); two launches lost everywhere (gate+up at M = 16: 50.1
-// vs 47.2 us).  Where the decode kernel does not take the shape, the CUDA-core
-// kernel reads the weights once per two rows of x and wins up to M = 2, or up
-// to M = 6 for layers of N >= 9424 outputs.
+// (qmm), measured on GB300 in-stream at b = 4 for the Llama-3.1-8B shapes and
+// the 3B gate+up and down, g = 32 / 64 / 128, M = 2..16.  The tensor-core
+// decode kernel reads the weights once per launch of up to 2 (g = 32), 4
+// (g = 64) or 8 (g >= 128) rows of x, so its time grows with the launches
+// ("passes"); qmm's is nearly flat in M but grows as g shrinks (a K step of
+// 128 codes has 128 / g groups to rescale): gate+up takes 47 / 78 / 141 us at
+// g = 128 / 64 / 32.  The decode path wins up to 128 / g passes (M <= 8 for
+// g <= 128): e.g. g = 32 gate+up at M = 4: 30 against 141 us; g = 64 o at
+// M = 8: 11.4 against 15.0 us.  For N >= 24576 (gate+up: qmm runs 232 row
+// tiles, a second wave on 80 of the 152 SMs) twice as many passes still win
+// (g = 128 at M = 12 / 16: 37.6 / 44.4 against 46.9 / 47.1 us).  With
+// K > 8192 the decode kernel splits K over clusters of three or more CTAs and
+// loses beyond 4 / 6 / 8 rows at g = 128 / 64 / 32 (down at g = 128, M = 5:
+// 26.4 against 24.1 us; g = 64, M = 8: 35.8 against 32.2 us).  Where the
+// decode kernel does not take the shape, the CUDA-core kernel reads the
+// weights once per two rows of x and wins up to M = 2, or up to M = 6 for
+// layers of N >= 9424 outputs.
 constexpr int64_t kQmvMaxM = 2;
 constexpr int64_t kQmvMaxMWide = 6;
 constexpr int64_t kWideN = 9424;          // 76 row tiles of 124: half the SMs
 constexpr int64_t kClusterK = 8192;       // above: the decode kernel splits K over >= 3 CTAs
-constexpr int64_t kClusterMaxM = 4;       // ... and loses to qmm beyond this many rows
+constexpr int64_t kTwoWaveN = 24576;      // qmm needs more than one wave of row tiles at M <= 128
+
+// Decode passes that still beat qmm, and rows of x beyond which a K split over
+// clusters loses.  (Group 256 keeps one pass: its qmm rescales once per two K
+// steps, and its two-pass crossover was not measured.)
+int64_t decode_max_passes(int group, int64_t N) {
+    const int64_t p = group >= 128 ? 1 : 128 / group;
+    return (N >= kTwoWaveN && group <= 128) ? 2 * p : p;
+}
+int64_t cluster_max_rows(int group) { return group >= 128 ? 4 : (group == 64 ? 6 : 8); }
 
 }  // namespace
 
@@ -168,7 +185,8 @@ lowbit_path lowbit_select_path(int64_t M, int64_t K, int64_t N, int bits, int gr
     if (lowbit::qmv_mma_shape_ok(K, group)) {
         const int64_t rows = lowbit::qmv_mma_rows(group);
         const int64_t passes = (M + rows - 1) / rows;
-        return (passes <= 1 && !(K > kClusterK && M > kClusterMaxM)) ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
+        return (passes <= decode_max_passes(group, N) && !(K > kClusterK && M > cluster_max_rows(group)))
+                   ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
     }
     return (M <= kQmvMaxM || (M <= kQmvMaxMWide && N >= kWideN)) ? LOWBIT_PATH_QMV : LOWBIT_PATH_QMM;
 }

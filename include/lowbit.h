@@ -212,11 +212,13 @@ LOWBIT_API lowbit_status lowbit_linear_swiglu(const uint16_t *x, const uint8_t *
                                    lowbit_stream_t stream);
 
 /* The kernel lowbit_linear runs for this problem, from crossovers measured on
- * GB300: LOWBIT_PATH_QMV when the tensor-core decode kernel covers M in one
- * launch (K a multiple of 256 up to 32768 with K/group a multiple of 8:
- * M <= 2 for group 32, M <= 4 for group 64, M <= 8 for groups 128 and 256),
- * except M > 4 with K > 8192; for other K, M <= 2, or M <= 6 when
- * N >= 9424; and whenever K is not a multiple of 128.
+ * GB300: LOWBIT_PATH_QMV when the tensor-core decode kernel takes the shape
+ * (K a multiple of 256 up to 32768 with K/group a multiple of 8; one launch
+ * per 2 rows of x for group 32, 4 for group 64, 8 for groups 128 and 256) in
+ * at most 128/group launches (one for groups 128 and 256), twice as many when
+ * N >= 24576 and group <= 128, and, when K > 8192, for M <= 4 (groups 128,
+ * 256), 6 (64) or 8 (32); for other K, M <= 2, or M <= 6 when N >= 9424; and
+ * whenever K is not a multiple of 128.
  * LOWBIT_PATH_QMM otherwise.  The choice assumes x, the packed weights,
  * scales and zeros 16-byte aligned (the decode path still runs, slower,
  * when they are not).

@@ -69,20 +69,34 @@ def test_select_path(lib):
     assert lb.select_path(0, 4096, 4096, 4, 64) == lb.PATH_QMV
     assert lb.select_path(128, 4096, 4096, 4, 64) == lb.PATH_QMM
     # Measured crossovers.  The tensor-core decode kernel takes 2 / 4 / 8 rows of x
-    # per launch for g = 32 / 64 / >= 128: one launch, except above 4 rows when
-    # K > 8192 (split over clusters of three or more CTAs); never two.
-    assert lb.select_path(4, 4096, 4096, 4, 64) == lb.PATH_QMV
-    assert lb.select_path(5, 4096, 4096, 4, 64) == lb.PATH_QMM
+    # per launch for g = 32 / 64 / >= 128 and wins in up to 128 / g launches (one
+    # for g >= 128), twice as many for N >= 24576; with K > 8192 (K split over
+    # clusters of three or more CTAs) only up to 4 / 6 / 8 rows.
+    assert lb.select_path(8, 4096, 4096, 4, 64) == lb.PATH_QMV        # 2 launches
+    assert lb.select_path(9, 4096, 4096, 4, 64) == lb.PATH_QMM
     assert lb.select_path(8, 4096, 6144, 4, 128) == lb.PATH_QMV
     assert lb.select_path(9, 4096, 6144, 4, 128) == lb.PATH_QMM
     assert lb.select_path(4, 14336, 4096, 7, 256) == lb.PATH_QMV
     assert lb.select_path(5, 14336, 4096, 7, 256) == lb.PATH_QMM
+    assert lb.select_path(4, 14336, 4096, 4, 128) == lb.PATH_QMV
+    assert lb.select_path(5, 14336, 4096, 4, 128) == lb.PATH_QMM
+    assert lb.select_path(6, 14336, 4096, 4, 64) == lb.PATH_QMV
+    assert lb.select_path(7, 14336, 4096, 4, 64) == lb.PATH_QMM
+    assert lb.select_path(8, 14336, 4096, 4, 32) == lb.PATH_QMV
+    assert lb.select_path(9, 14336, 4096, 4, 32) == lb.PATH_QMM
     assert lb.select_path(8, 8192, 3072, 4, 128) == lb.PATH_QMV
-    assert lb.select_path(2, 4096, 4096, 4, 32) == lb.PATH_QMV
-    assert lb.select_path(3, 4096, 4096, 4, 32) == lb.PATH_QMM
-    assert lb.select_path(8, 4096, 28672, 4, 128) == lb.PATH_QMV
-    assert lb.select_path(9, 4096, 28672, 4, 128) == lb.PATH_QMM
+    assert lb.select_path(8, 8192, 3072, 4, 32) == lb.PATH_QMV        # K = 8192: no row cap
+    assert lb.select_path(8, 4096, 4096, 4, 32) == lb.PATH_QMV        # 4 launches
+    assert lb.select_path(9, 4096, 4096, 4, 32) == lb.PATH_QMM
+    assert lb.select_path(16, 4096, 28672, 4, 128) == lb.PATH_QMV     # 2 launches, N >= 24576
+    assert lb.select_path(17, 4096, 28672, 4, 128) == lb.PATH_QMM
+    assert lb.select_path(16, 4096, 28672, 4, 64) == lb.PATH_QMV      # 4 launches
+    assert lb.select_path(17, 4096, 28672, 4, 64) == lb.PATH_QMM
+    assert lb.select_path(16, 4096, 28672, 4, 32) == lb.PATH_QMV      # 8 launches
+    assert lb.select_path(17, 4096, 28672, 4, 32) == lb.PATH_QMM
+    assert lb.select_path(9, 4096, 16384, 4, 128) == lb.PATH_QMM
     assert lb.select_path(16, 4096, 16384, 4, 128) == lb.PATH_QMM
+    assert lb.select_path(9, 4096, 28672, 7, 256) == lb.PATH_QMM      # g = 256: one launch
     # Shapes the decode kernel does not take: the CUDA-core kernel's crossover
     # (K % 256 != 0; K / group not a multiple of 8).
     assert lb.select_path(2, 4096 + 128, 4096, 4, 64) == lb.PATH_QMV
