@@ -31,20 +31,25 @@
 // The codes are written packed (contiguous, LSB-first, ao PR #2167 Summary
 // bullet 2).
 //
-// Work unit: one warp per chunk of 256 consecutive weights of a row.  Lane l
-// takes weights [8l, 8l+8); a group of g weights spans g/8 lanes, whose
-// min/max is a segmented shuffle reduction; the lane's 8 codes are one octet,
-// written as b bytes at byte l*b of the chunk's packed bytes.  The weights
-// arrive through a per-warp ring of 8 chunks in shared memory, filled with
-// 16-byte asynchronous copies (cp.async) 7 chunks ahead of the one being
-// coded, so that each warp keeps several KB of loads in flight.
+// Work unit: one warp per chunk of 512 consecutive weights of a row.  Lane l
+// takes weights [16l, 16l+16); a group of g weights spans g/16 lanes, whose
+// min/max is a segmented shuffle reduction; the lane's 16 codes are two
+// octets, written as 2b bytes at byte 2lb of the chunk's packed bytes.  (Eight
+// weights a lane cost 240 instructions per 256 weights, more than half of them
+// per chunk rather than per weight: prefetch bookkeeping, the group reductions,
+// the scale and its broadcast, indices and stores.)  The weights arrive through
+// a per-warp ring in shared memory of 8 chunks (16-bit inputs) or 4 (fp32),
+// filled with 16-byte asynchronous copies (cp.async) that many chunks ahead of
+// the one being coded, less one, so that each warp keeps several KB of loads
+// in flight.
 #include "common.cuh"
 
 namespace lowbit {
 namespace {
 
-constexpr int kChunk = 256;          // weights per warp per step
-constexpr int kRing = 8;             // chunks of a warp in flight (shared-memory ring)
+constexpr int kPerLane = 16;         // weights per lane per step
+constexpr int kChunk = 32 * kPerLane; // weights per warp per step
+constexpr int kRingBytes = 8192;     // a warp's shared-memory ring: 8 chunks of 16-bit weights, 4 of fp32
 constexpr int kWarps = 8;            // warps per block
 
 struct W8 {
@@ -203,14 +208,14 @@ struct Octet {
     }
 };
 
-// GL = lanes per group (g / 8): 4, 8, 16 or 32.  WIDE: the packed matrix is
+// GL = lanes per group (g / 16): 2, 4, 8 or 16.  WIDE: the packed matrix is
 // aligned for the 16- and 32-bit stores of b = 2, 4, 6 (it may have any
 // alignment; otherwise every byte is stored on its own).
 template <int BITS, int GL, bool WIDE>
 __global__ void __launch_bounds__(256, 3)
 quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ packed,
                 uint16_t *__restrict__ scales, uint16_t *__restrict__ zeros, int64_t N, int K) {
-    constexpr int group = GL * 8;
+    constexpr int group = GL * kPerLane;
     constexpr float qmax = (float)((1 << BITS) - 1);
     const float rq_lo = __frcp_rd(qmax), rq_hi = __frcp_ru(qmax);
     const int lane = threadIdx.x & 31;
@@ -220,12 +225,14 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
     const int64_t row_bytes = (int64_t)K * BITS / 8;
 
-    // The warp's ring: kRing slots of 32 lanes x 32 bytes (16-bit inputs use
-    // the first 16 bytes of a lane's 32).
-    __shared__ __align__(16) uint8_t ring[kWarps][kRing][32 * 32];
+    // The warp's ring: R slots of 32 lanes x 16 weights (R = 8 for 16-bit
+    // inputs, 4 for fp32).
+    __shared__ __align__(16) uint8_t ring[kWarps][kRingBytes];
     const int wib = threadIdx.x >> 5;
-    const uint32_t ring0 = (uint32_t)__cvta_generic_to_shared(&ring[wib][0][lane * 32]);
     const int esz = dtype == LOWBIT_DTYPE_F32 ? 4 : 2;
+    const int lane_bytes = kPerLane * esz;
+    const int R = kRingBytes / (32 * lane_bytes);
+    const uint32_t ring0 = (uint32_t)__cvta_generic_to_shared(&ring[wib][lane * lane_bytes]);
 
     int64_t c = (int64_t)blockIdx.x * (blockDim.x / 32) + wib;
     if (c >= chunks) return;                                 // whole warp leaves together
@@ -235,20 +242,19 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
     const int dc = (int)(warps % cpr);
     int64_t n = c / cpr;
     int kc = (int)(c - n * cpr);
-    int k = kc * kChunk + lane * 8;
-    // Prefetch cursor: kRing - 1 chunks ahead of (c, n, kc), each copy group
+    int k = kc * kChunk + lane * kPerLane;
+    // Prefetch cursor: R - 1 chunks ahead of (c, n, kc), each copy group
     // committed whether or not it copies anything, so that waiting for all but
-    // the newest kRing - 1 groups always means "this chunk has landed".
+    // the newest R - 1 groups always means "this chunk has landed".
     int64_t cp_c = c, cp_n = n;
     int cp_kc = kc;
     auto issue = [&](int slot) {
-        const int kk = cp_kc * kChunk + lane * 8;
+        const int kk = cp_kc * kChunk + lane * kPerLane;
         if (cp_c < chunks) {
             const uint8_t *src = reinterpret_cast<const uint8_t *>(w) + (cp_n * K + kk) * esz;
             const uint32_t nb = kk < K ? 16u : 0u;
-            const uint32_t dst = ring0 + (uint32_t)(slot * 32 * 32);
-            cp_async16(dst, kk < K ? src : w, nb);
-            if (esz == 4) cp_async16(dst + 16, kk < K ? src + 16 : w, nb);
+            const uint32_t dst = ring0 + (uint32_t)(slot * 32 * lane_bytes);
+            for (int j = 0; j < lane_bytes; j += 16) cp_async16(dst + j, kk < K ? src + j : w, nb);
         }
         cp_async_commit();
         cp_c += warps;
@@ -256,27 +262,29 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
         cp_kc += dc;
         if (cp_kc >= cpr) { cp_kc -= cpr; ++cp_n; }
     };
-#pragma unroll
-    for (int j = 0; j < kRing - 1; ++j) issue(j);
+    for (int j = 0; j < R - 1; ++j) issue(j);
     int slot = 0;                                        // ring slot of this chunk
     for (; c < chunks; c += warps) {
-        issue(slot == 0 ? kRing - 1 : slot - 1);         // into the slot read last iteration
-        cp_async_wait<kRing - 1>();                      // this chunk's copies have landed
-        const uint8_t *mine = &ring[wib][slot][lane * 32];
-        if (++slot == kRing) slot = 0;
-        const W8 cur = convert8(dtype, *reinterpret_cast<const uint4 *>(mine),
-                                *reinterpret_cast<const uint4 *>(mine + 16));
+        issue(slot == 0 ? R - 1 : slot - 1);             // into the slot read last iteration
+        if (esz == 4) cp_async_wait<3>();                // this chunk's copies have landed
+        else cp_async_wait<7>();
+        const uint8_t *mine = &ring[wib][slot * 32 * lane_bytes + lane * lane_bytes];
+        if (++slot == R) slot = 0;
+        // The lane's weights 0..7 (wa) and 8..15 (wb).
+        const uint4 *u = reinterpret_cast<const uint4 *>(mine);
+        const W8 wa = esz == 4 ? convert8(dtype, u[0], u[1]) : convert8(dtype, u[0], u[0]);
+        const W8 wb = esz == 4 ? convert8(dtype, u[2], u[3]) : convert8(dtype, u[1], u[1]);
         int64_t n2 = n + dn;
         int kc2 = kc + dc;
         if (kc2 >= cpr) { kc2 -= cpr; ++n2; }
-        const int k2 = kc2 * kChunk + lane * 8;
+        const int k2 = kc2 * kChunk + lane * kPerLane;
         // A group lies wholly inside or wholly outside the row (K % group == 0),
         // so lanes past the row end only ever reduce among themselves.
-        float mn = cur.v[0], mx = cur.v[0];
+        float mn = fminf(wa.v[0], wb.v[0]), mx = fmaxf(wa.v[0], wb.v[0]);
 #pragma unroll
         for (int i = 1; i < 8; ++i) {
-            mn = fminf(mn, cur.v[i]);
-            mx = fmaxf(mx, cur.v[i]);
+            mn = fminf(mn, fminf(wa.v[i], wb.v[i]));
+            mx = fmaxf(mx, fmaxf(wa.v[i], wb.v[i]));
         }
 #pragma unroll
         for (int o = 1; o < GL; o <<= 1) {
@@ -288,10 +296,10 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
         if (__any_sync(0xffffffffu, mn == 0.0f)) {
             uint32_t key = 0xFFFFFFFFu;                       // (position << 1) | sign
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (cur.v[i] == 0.0f)
-                    key = min(key, ((uint32_t)(lane * 8 + i) << 1) |
-                                       (__float_as_uint(cur.v[i]) >> 31));
+            for (int i = 0; i < kPerLane; ++i) {
+                const float vi = i < 8 ? wa.v[i] : wb.v[i - 8];
+                if (vi == 0.0f) key = min(key, ((uint32_t)(lane * kPerLane + i) << 1) | (__float_as_uint(vi) >> 31));
+            }
 #pragma unroll
             for (int o = 1; o < GL; o <<= 1)
                 key = min(key, __shfl_xor_sync(0xffffffffu, key, o));
@@ -309,30 +317,43 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
         if (k < K) {
             const float s = __half2float(__ushort_as_half(sh));
             const float inv_s = __frcp_rn(s);
-            Octet<BITS> o;
+            Octet<BITS> o0, o1;
             if (!flat) {
                 uint32_t q[8];
-                codes8(cur.v, z, s, inv_s, q);
                 // The mask changes no valid code; it keeps a NaN weight's
                 // code (0, as before) from spilling into its neighbours.
+                codes8(wa.v, z, s, inv_s, q);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) o.put(i, q[i] & ((1u << BITS) - 1u));
+                for (int i = 0; i < 8; ++i) o0.put(i, q[i] & ((1u << BITS) - 1u));
+                codes8(wb.v, z, s, inv_s, q);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o1.put(i, q[i] & ((1u << BITS) - 1u));
             }
             uint8_t *dst = packed + n * row_bytes + (int64_t)(k / 8) * BITS;
-            // b bytes at byte (k / 8) b of the row: one 32-bit store for b = 4,
-            // 16-bit stores for b = 2 and 6 (row and octet offsets are multiples
-            // of 4 and 2 bytes), bytes otherwise or when the matrix is not aligned.
+            // 2b bytes at byte (k / 8) b of the row, octet 0 then octet 1:
+            // 32-bit stores for b = 4, 16-bit stores for b = 2 and 6 (row and
+            // octet offsets are multiples of 4 and 2 bytes), bytes otherwise or
+            // when the matrix is not aligned.
             if constexpr (WIDE && BITS == 4) {
-                *reinterpret_cast<uint32_t *>(dst) = o.lo;
+                reinterpret_cast<uint32_t *>(dst)[0] = o0.lo;
+                reinterpret_cast<uint32_t *>(dst)[1] = o1.lo;
             } else if constexpr (WIDE && BITS == 2) {
-                *reinterpret_cast<uint16_t *>(dst) = (uint16_t)o.lo;
+                reinterpret_cast<uint16_t *>(dst)[0] = (uint16_t)o0.lo;
+                reinterpret_cast<uint16_t *>(dst)[1] = (uint16_t)o1.lo;
             } else if constexpr (WIDE && BITS == 6) {
-                reinterpret_cast<uint16_t *>(dst)[0] = (uint16_t)o.lo;
-                reinterpret_cast<uint16_t *>(dst)[1] = (uint16_t)(o.lo >> 16);
-                reinterpret_cast<uint16_t *>(dst)[2] = (uint16_t)o.hi;
+                uint16_t *d16 = reinterpret_cast<uint16_t *>(dst);
+                d16[0] = (uint16_t)o0.lo;
+                d16[1] = (uint16_t)(o0.lo >> 16);
+                d16[2] = (uint16_t)o0.hi;
+                d16[3] = (uint16_t)o1.lo;
+                d16[4] = (uint16_t)(o1.lo >> 16);
+                d16[5] = (uint16_t)o1.hi;
             } else {
 #pragma unroll
-                for (int i = 0; i < BITS; ++i) dst[i] = o.byte(i);
+                for (int i = 0; i < BITS; ++i) {
+                    dst[i] = o0.byte(i);
+                    dst[BITS + i] = o1.byte(i);
+                }
             }
             if ((lane & (GL - 1)) == 0) {
                 const int64_t gi = n * G + k / group;
@@ -369,10 +390,10 @@ template <int BITS, bool WIDE>
 cudaError_t launch_group(const void *w, int dtype, uint8_t *packed, uint16_t *scales,
                          uint16_t *zeros, int64_t N, int K, int group, cudaStream_t stream) {
     switch (group) {
-        case 32: return launch_one<BITS, 4, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
-        case 64: return launch_one<BITS, 8, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
-        case 128: return launch_one<BITS, 16, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
-        case 256: return launch_one<BITS, 32, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 32: return launch_one<BITS, 2, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 64: return launch_one<BITS, 4, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 128: return launch_one<BITS, 8, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 256: return launch_one<BITS, 16, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
         default: return cudaErrorInvalidValue;
     }
 }
