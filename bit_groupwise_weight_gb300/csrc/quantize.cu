@@ -31,25 +31,27 @@
 // The codes are written packed (contiguous, LSB-first, ao PR #2167 Summary
 // bullet 2).
 //
-// Work unit: one warp per chunk of 512 consecutive weights of a row.  Lane l
-// takes weights [16l, 16l+16); a group of g weights spans g/16 lanes, whose
-// min/max is a segmented shuffle reduction; the lane's 16 codes are two
-// octets, written as 2b bytes at byte 2lb of the chunk's packed bytes.  (Eight
-// weights a lane cost 240 instructions per 256 weights, more than half of them
-// per chunk rather than per weight: prefetch bookkeeping, the group reductions,
-// the scale and its broadcast, indices and stores.)  The weights arrive through
-// a per-warp ring in shared memory of 8 chunks (16-bit inputs) or 4 (fp32),
-// filled with 16-byte asynchronous copies (cp.async) that many chunks ahead of
-// the one being coded, less one, so that each warp keeps several KB of loads
-// in flight.
+// Work unit: one warp per chunk of 1024 consecutive weights of a row.  Lane l
+// takes weights [32l, 32l+32); a group of g weights spans g/32 lanes (one lane
+// for g = 32), whose min/max is a segmented shuffle reduction; the lane's 32
+// codes are four octets, written as 4b bytes at byte 4lb of the chunk's packed
+// bytes.  (Eight weights a lane cost 240 instructions per 256 weights, more
+// than half of them per chunk rather than per weight: prefetch bookkeeping, the
+// group reductions, the scale and its broadcast, indices and stores.)  The
+// weights arrive through a per-warp ring in shared memory of 4 chunks (16-bit
+// inputs) or 2 (fp32), filled with 16-byte asynchronous copies (cp.async) that
+// many chunks ahead of the one being coded, less one, so that each warp keeps
+// several KB of loads in flight; a lane reads its weights from the ring twice
+// (for the group's min/max, then for the codes) rather than holding 32 values.
 #include "common.cuh"
 
 namespace lowbit {
 namespace {
 
-constexpr int kPerLane = 16;         // weights per lane per step
+constexpr int kPerLane = 32;         // weights per lane per step
+constexpr int kOct = kPerLane / 8;   // octets (blocks of 8 weights) per lane
 constexpr int kChunk = 32 * kPerLane; // weights per warp per step
-constexpr int kRingBytes = 8192;     // a warp's shared-memory ring: 8 chunks of 16-bit weights, 4 of fp32
+constexpr int kRingBytes = 8192;     // a warp's shared-memory ring: 4 chunks of 16-bit weights, 2 of fp32
 constexpr int kWarps = 8;            // warps per block
 
 struct W8 {
@@ -208,7 +210,7 @@ struct Octet {
     }
 };
 
-// GL = lanes per group (g / 16): 2, 4, 8 or 16.  WIDE: the packed matrix is
+// GL = lanes per group (g / 32): 1, 2, 4 or 8.  WIDE: the packed matrix is
 // aligned for the 16- and 32-bit stores of b = 2, 4, 6 (it may have any
 // alignment; otherwise every byte is stored on its own).
 template <int BITS, int GL, bool WIDE>
@@ -225,8 +227,8 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
     const int64_t row_bytes = (int64_t)K * BITS / 8;
 
-    // The warp's ring: R slots of 32 lanes x 16 weights (R = 8 for 16-bit
-    // inputs, 4 for fp32).
+    // The warp's ring: R slots of 32 lanes x 32 weights (R = 4 for 16-bit
+    // inputs, 2 for fp32).
     __shared__ __align__(16) uint8_t ring[kWarps][kRingBytes];
     const int wib = threadIdx.x >> 5;
     const int esz = dtype == LOWBIT_DTYPE_F32 ? 4 : 2;
@@ -266,25 +268,40 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
     int slot = 0;                                        // ring slot of this chunk
     for (; c < chunks; c += warps) {
         issue(slot == 0 ? R - 1 : slot - 1);             // into the slot read last iteration
-        if (esz == 4) cp_async_wait<3>();                // this chunk's copies have landed
-        else cp_async_wait<7>();
+        if (esz == 4) cp_async_wait<1>();                // this chunk's copies have landed
+        else cp_async_wait<3>();
         const uint8_t *mine = &ring[wib][slot * 32 * lane_bytes + lane * lane_bytes];
         if (++slot == R) slot = 0;
-        // The lane's weights 0..7 (wa) and 8..15 (wb).
+        // Block h of the lane's weights: 8 weights from the ring (16 or 32 bytes).
         const uint4 *u = reinterpret_cast<const uint4 *>(mine);
-        const W8 wa = esz == 4 ? convert8(dtype, u[0], u[1]) : convert8(dtype, u[0], u[0]);
-        const W8 wb = esz == 4 ? convert8(dtype, u[2], u[3]) : convert8(dtype, u[1], u[1]);
+        auto block = [&](int h) {
+            return esz == 4 ? convert8(dtype, u[2 * h], u[2 * h + 1]) : convert8(dtype, u[h], u[h]);
+        };
         int64_t n2 = n + dn;
         int kc2 = kc + dc;
         if (kc2 >= cpr) { kc2 -= cpr; ++n2; }
         const int k2 = kc2 * kChunk + lane * kPerLane;
         // A group lies wholly inside or wholly outside the row (K % group == 0),
         // so lanes past the row end only ever reduce among themselves.
-        float mn = fminf(wa.v[0], wb.v[0]), mx = fmaxf(wa.v[0], wb.v[0]);
+        float mn, mx;
+        {
+            const W8 b0 = block(0);
+            mn = b0.v[0];
+            mx = b0.v[0];
 #pragma unroll
-        for (int i = 1; i < 8; ++i) {
-            mn = fminf(mn, fminf(wa.v[i], wb.v[i]));
-            mx = fmaxf(mx, fmaxf(wa.v[i], wb.v[i]));
+            for (int i = 1; i < 8; ++i) {
+                mn = fminf(mn, b0.v[i]);
+                mx = fmaxf(mx, b0.v[i]);
+            }
+        }
+#pragma unroll
+        for (int h = 1; h < kOct; ++h) {
+            const W8 bh = block(h);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                mn = fminf(mn, bh.v[i]);
+                mx = fmaxf(mx, bh.v[i]);
+            }
         }
 #pragma unroll
         for (int o = 1; o < GL; o <<= 1) {
@@ -296,9 +313,12 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
         if (__any_sync(0xffffffffu, mn == 0.0f)) {
             uint32_t key = 0xFFFFFFFFu;                       // (position << 1) | sign
 #pragma unroll
-            for (int i = 0; i < kPerLane; ++i) {
-                const float vi = i < 8 ? wa.v[i] : wb.v[i - 8];
-                if (vi == 0.0f) key = min(key, ((uint32_t)(lane * kPerLane + i) << 1) | (__float_as_uint(vi) >> 31));
+            for (int h = 0; h < kOct; ++h) {
+                const W8 bh = block(h);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (bh.v[i] == 0.0f)
+                        key = min(key, ((uint32_t)(lane * kPerLane + 8 * h + i) << 1) | (__float_as_uint(bh.v[i]) >> 31));
             }
 #pragma unroll
             for (int o = 1; o < GL; o <<= 1)
@@ -317,42 +337,38 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
         if (k < K) {
             const float s = __half2float(__ushort_as_half(sh));
             const float inv_s = __frcp_rn(s);
-            Octet<BITS> o0, o1;
+            Octet<BITS> o[kOct];
             if (!flat) {
-                uint32_t q[8];
-                // The mask changes no valid code; it keeps a NaN weight's
-                // code (0, as before) from spilling into its neighbours.
-                codes8(wa.v, z, s, inv_s, q);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) o0.put(i, q[i] & ((1u << BITS) - 1u));
-                codes8(wb.v, z, s, inv_s, q);
+                for (int h = 0; h < kOct; ++h) {
+                    uint32_t q[8];
+                    codes8(block(h).v, z, s, inv_s, q);
+                    // The mask changes no valid code; it keeps a NaN weight's
+                    // code (0, as before) from spilling into its neighbours.
 #pragma unroll
-                for (int i = 0; i < 8; ++i) o1.put(i, q[i] & ((1u << BITS) - 1u));
+                    for (int i = 0; i < 8; ++i) o[h].put(i, q[i] & ((1u << BITS) - 1u));
+                }
             }
             uint8_t *dst = packed + n * row_bytes + (int64_t)(k / 8) * BITS;
-            // 2b bytes at byte (k / 8) b of the row, octet 0 then octet 1:
+            // kOct b bytes at byte (k / 8) b of the row, octet after octet:
             // 32-bit stores for b = 4, 16-bit stores for b = 2 and 6 (row and
             // octet offsets are multiples of 4 and 2 bytes), bytes otherwise or
             // when the matrix is not aligned.
-            if constexpr (WIDE && BITS == 4) {
-                reinterpret_cast<uint32_t *>(dst)[0] = o0.lo;
-                reinterpret_cast<uint32_t *>(dst)[1] = o1.lo;
-            } else if constexpr (WIDE && BITS == 2) {
-                reinterpret_cast<uint16_t *>(dst)[0] = (uint16_t)o0.lo;
-                reinterpret_cast<uint16_t *>(dst)[1] = (uint16_t)o1.lo;
-            } else if constexpr (WIDE && BITS == 6) {
-                uint16_t *d16 = reinterpret_cast<uint16_t *>(dst);
-                d16[0] = (uint16_t)o0.lo;
-                d16[1] = (uint16_t)(o0.lo >> 16);
-                d16[2] = (uint16_t)o0.hi;
-                d16[3] = (uint16_t)o1.lo;
-                d16[4] = (uint16_t)(o1.lo >> 16);
-                d16[5] = (uint16_t)o1.hi;
-            } else {
 #pragma unroll
-                for (int i = 0; i < BITS; ++i) {
-                    dst[i] = o0.byte(i);
-                    dst[BITS + i] = o1.byte(i);
+            for (int h = 0; h < kOct; ++h) {
+                uint8_t *dh = dst + h * BITS;
+                if constexpr (WIDE && BITS == 4) {
+                    *reinterpret_cast<uint32_t *>(dh) = o[h].lo;
+                } else if constexpr (WIDE && BITS == 2) {
+                    *reinterpret_cast<uint16_t *>(dh) = (uint16_t)o[h].lo;
+                } else if constexpr (WIDE && BITS == 6) {
+                    uint16_t *d16 = reinterpret_cast<uint16_t *>(dh);
+                    d16[0] = (uint16_t)o[h].lo;
+                    d16[1] = (uint16_t)(o[h].lo >> 16);
+                    d16[2] = (uint16_t)o[h].hi;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < BITS; ++i) dh[i] = o[h].byte(i);
                 }
             }
             if ((lane & (GL - 1)) == 0) {
@@ -390,10 +406,10 @@ template <int BITS, bool WIDE>
 cudaError_t launch_group(const void *w, int dtype, uint8_t *packed, uint16_t *scales,
                          uint16_t *zeros, int64_t N, int K, int group, cudaStream_t stream) {
     switch (group) {
-        case 32: return launch_one<BITS, 2, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
-        case 64: return launch_one<BITS, 4, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
-        case 128: return launch_one<BITS, 8, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
-        case 256: return launch_one<BITS, 16, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 32: return launch_one<BITS, 1, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 64: return launch_one<BITS, 2, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 128: return launch_one<BITS, 4, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
+        case 256: return launch_one<BITS, 8, WIDE>(w, dtype, packed, scales, zeros, N, K, stream);
         default: return cudaErrorInvalidValue;
     }
 }
