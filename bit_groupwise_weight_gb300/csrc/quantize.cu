@@ -83,6 +83,37 @@ __device__ __forceinline__ W8 convert8(int dtype, uint4 u, uint4 u2) {
     return r;
 }
 
+// Packed minimum / maximum of two bf16 or two fp16 pairs: exact, and a NaN
+// input yields the other input, as fminf / fmaxf do.
+__device__ __forceinline__ uint32_t min_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t min_f16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t max_f16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// 16 bytes of shared memory, loaded where it is written (volatile: the
+// weights are read twice from the ring, rather than held in registers).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
 // 16-byte asynchronous copy global -> shared (L2 only); src_bytes 0 fills zeros.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -270,12 +301,13 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
         issue(slot == 0 ? R - 1 : slot - 1);             // into the slot read last iteration
         if (esz == 4) cp_async_wait<1>();                // this chunk's copies have landed
         else cp_async_wait<3>();
-        const uint8_t *mine = &ring[wib][slot * 32 * lane_bytes + lane * lane_bytes];
+        const uint32_t mine = ring0 + (uint32_t)(slot * 32 * lane_bytes);
         if (++slot == R) slot = 0;
         // Block h of the lane's weights: 8 weights from the ring (16 or 32 bytes).
-        const uint4 *u = reinterpret_cast<const uint4 *>(mine);
         auto block = [&](int h) {
-            return esz == 4 ? convert8(dtype, u[2 * h], u[2 * h + 1]) : convert8(dtype, u[h], u[h]);
+            if (esz == 4) return convert8(dtype, lds128(mine + 32u * h), lds128(mine + 32u * h + 16u));
+            const uint4 a = lds128(mine + 16u * h);
+            return convert8(dtype, a, a);
         };
         int64_t n2 = n + dn;
         int kc2 = kc + dc;
@@ -284,7 +316,35 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
         // A group lies wholly inside or wholly outside the row (K % group == 0),
         // so lanes past the row end only ever reduce among themselves.
         float mn, mx;
-        {
+        if (esz == 2) {
+            // 16-bit weights: packed minimum and maximum of the raw pairs,
+            // then of the two halves (the signs of zeros do not matter here:
+            // a zero minimum's sign is settled below, and the maximum only
+            // enters as max - zero).
+            const uint4 u0 = lds128(mine), u1 = lds128(mine + 16u), u2 = lds128(mine + 32u), u3 = lds128(mine + 48u);
+            const uint32_t wd[16] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w,
+                                     u2.x, u2.y, u2.z, u2.w, u3.x, u3.y, u3.z, u3.w};
+            uint32_t lo2 = wd[0], hi2 = wd[0];
+            if (dtype == LOWBIT_DTYPE_BF16) {
+#pragma unroll
+                for (int i = 1; i < 16; ++i) {
+                    lo2 = min_bf16x2(lo2, wd[i]);
+                    hi2 = max_bf16x2(hi2, wd[i]);
+                }
+                mn = fminf(__uint_as_float(lo2 << 16), __uint_as_float(lo2 & 0xFFFF0000u));
+                mx = fmaxf(__uint_as_float(hi2 << 16), __uint_as_float(hi2 & 0xFFFF0000u));
+            } else {
+#pragma unroll
+                for (int i = 1; i < 16; ++i) {
+                    lo2 = min_f16x2(lo2, wd[i]);
+                    hi2 = max_f16x2(hi2, wd[i]);
+                }
+                mn = fminf(__half2float(__ushort_as_half((uint16_t)(lo2 & 0xFFFFu))),
+                           __half2float(__ushort_as_half((uint16_t)(lo2 >> 16))));
+                mx = fmaxf(__half2float(__ushort_as_half((uint16_t)(hi2 & 0xFFFFu))),
+                           __half2float(__ushort_as_half((uint16_t)(hi2 >> 16))));
+            }
+        } else {
             const W8 b0 = block(0);
             mn = b0.v[0];
             mx = b0.v[0];
@@ -293,14 +353,14 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
                 mn = fminf(mn, b0.v[i]);
                 mx = fmaxf(mx, b0.v[i]);
             }
-        }
 #pragma unroll
-        for (int h = 1; h < kOct; ++h) {
-            const W8 bh = block(h);
+            for (int h = 1; h < kOct; ++h) {
+                const W8 bh = block(h);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                mn = fminf(mn, bh.v[i]);
-                mx = fmaxf(mx, bh.v[i]);
+                for (int i = 0; i < 8; ++i) {
+                    mn = fminf(mn, bh.v[i]);
+                    mx = fmaxf(mx, bh.v[i]);
+                }
             }
         }
 #pragma unroll
