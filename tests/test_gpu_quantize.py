@@ -66,6 +66,33 @@ def test_quantize_bit_exact(orc, dtype, bits, group):
     _check_exact(orc, w64, packed, scales, zeros, bits, group, f"{dtype} b={bits} g={group}")
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("bits", [1, 3, 4, 6, 7])
+@pytest.mark.parametrize("group", [32, 64, 128, 256])
+def test_quantize_rows_with_partial_chunk(orc, dtype, bits, group):
+    # Rows of one or more whole 1024-weight chunks of a warp and a partial
+    # last one (K = 1344 or 1280), so that consecutive chunks of a warp cross
+    # row ends at different offsets.
+    K = 1344 if group <= 64 else 1280
+    w32 = synth.make_weights(4, 29, K, key=(bits, group))
+    w_dev, w64 = _as_dtype(w32, dtype)
+    packed, scales, zeros = _gpu_quantize(w_dev, bits, group)
+    _check_exact(orc, w64, packed, scales, zeros, bits, group, f"partial {dtype} b={bits} g={group}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("bits", [3, 4])
+def test_quantize_warps_stride_across_rows(orc, dtype, bits):
+    # More chunks than resident warps, five chunks a row (K = 4416: four whole
+    # and one partial): each warp walks several chunks and its stride carries
+    # over row ends at changing chunk offsets.
+    K, N = 4416, 1000
+    w32 = synth.make_weights(5, N, K, key=(bits, 4416))
+    w_dev, w64 = _as_dtype(w32, dtype)
+    packed, scales, zeros = _gpu_quantize(w_dev, bits, 64)
+    _check_exact(orc, w64, packed, scales, zeros, bits, 64, f"stride {dtype} b={bits}")
+
+
 def _special_groups(bits: int, group: int) -> np.ndarray:
     """Rows of hand-built groups: each row is one group of `group` weights."""
     qmax = (1 << bits) - 1
