@@ -597,10 +597,15 @@ qmv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
                         }
                     }
                 }
-                __syncwarp();
-                // Hand the buffer back to every CTA of the cluster.
-                if (lane < ks)
-                    red_arrive(clustered, clustered ? ptx::mapa_shared(rfree0 + 8 * buf, (uint32_t)lane) : rfree0 + 8 * buf);
+                // Hand the buffer back to every CTA of the cluster, when a later
+                // stage reuses it (stage s + kRedBufs).  The arrive releases this
+                // warp's stores of y as well, so it is not made when nothing
+                // waits for it: it would only lengthen the call's tail.
+                if (s + kRedBufs < nst) {
+                    __syncwarp();
+                    if (lane < ks)
+                        red_arrive(clustered, clustered ? ptx::mapa_shared(rfree0 + 8 * buf, (uint32_t)lane) : rfree0 + 8 * buf);
+                }
             }
         }
     } else {
