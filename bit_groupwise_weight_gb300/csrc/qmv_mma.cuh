@@ -24,7 +24,8 @@
 //   under the fp32 rounding of the sum).
 //   The product (1024 + 2^p q) * 2^-p x' = q x' + 1024 2^-p x', so for every
 //   group the tensor cores return P' = sum q x' + O with O = sum 1024 2^-p x'
-//   (precomputed per warp from the same fp16 values), and
+//   (computed once per warp from the same fp16 B fragments, on the tensor
+//   cores as well: group_sums), and
 //     y = 2^-e * sum_g [ s (P' - O) + z X ],   X = sum x' over the group.
 //
 // Work split.  A consumer warp owns a 256-code slice of K (its B fragments
@@ -40,11 +41,13 @@
 // CTA = W consumer warps (K/ks = 256 W, W <= 16), one producer warp and one
 // finishing warp.  The producer copies each 16-row tile with 2D TMA tensor
 // copies (one box per part of the CTA's K range, as wide as the part plus its
-// row padding) into a ring of shared-memory stages (mbarrier completion).  Consumers reduce a tile's partial sums over the
-// four lanes of a row group with shuffles and store them, per warp, into a
-// reduction buffer of the cluster's first CTA (DSMEM); its finishing warp
-// adds the ks * W partials of every output in a fixed order, adds the bias,
-// rounds once to bf16 and stores y.  When K > 4096 the K range is split over
+// row padding) into a ring of shared-memory stages (mbarrier completion).
+// Consumers reduce a tile's partial sums over the four lanes of a row group
+// with shuffles and store them, per warp, into a reduction buffer of the
+// cluster's first CTA (DSMEM); its finishing warp adds the ks * W partials of
+// every output in a fixed order, adds the bias, rounds once to bf16 and stores
+// y (with 4 or 8 rows of x and at most two stages the first CTA's consumers
+// finish the last stage together).  When K > 4096 the K range is split over
 // the ks CTAs of a thread-block cluster; no global scratch memory is used.
 //
 // Every mbarrier wait is bounded (about one second) and counts a timeout
