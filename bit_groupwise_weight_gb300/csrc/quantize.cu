@@ -198,9 +198,12 @@ __device__ __noinline__ uint32_t code_near_tie(float v, float z, float s, uint32
 // Codes of a lane's 8 weights: rint(fl64(fl64(v - z) / s)) (see the header).
 // r = (v - z) * (1/s) in fp32; t = r + 2^23 rounds r to the nearest integer,
 // ties to even, into t's low mantissa bits (0 <= r < 2^22), so t's bits are
-// 0x4B000000 + code; r - (t - 2^23) is exact.  Weights whose r lies within
-// 2^-14 of a half-integer are recomputed in fp64.
-__device__ __forceinline__ void codes8(const float (&v)[8], float z, float s, float inv_s, uint32_t (&q)[8]) {
+// 0x4B000000 + code and the code is t's bits under the b-bit mask (0x4B000000
+// has none of them; a NaN weight's bits give the same masked code as before);
+// r - (t - 2^23) is exact.  Weights whose r lies within 2^-14 of a
+// half-integer are recomputed in fp64.
+__device__ __forceinline__ void codes8(const float (&v)[8], float z, float s, float inv_s, uint32_t mask,
+                                       uint32_t (&q)[8]) {
     const float2 z2 = make_float2(z, z), is2 = make_float2(inv_s, inv_s);
     const float2 big = make_float2(8388608.0f, 8388608.0f);
     float2 d[4];
@@ -210,8 +213,8 @@ __device__ __forceinline__ void codes8(const float (&v)[8], float z, float s, fl
         const float2 r = mul2(sub2(make_float2(v[2 * i], v[2 * i + 1]), z2), is2);
         const float2 t = add2(r, big);
         d[i] = sub2(r, sub2(t, big));
-        q[2 * i] = __float_as_uint(t.x) - 0x4B000000u;
-        q[2 * i + 1] = __float_as_uint(t.y) - 0x4B000000u;
+        q[2 * i] = __float_as_uint(t.x) & mask;
+        q[2 * i + 1] = __float_as_uint(t.y) & mask;
         near_tie |= fmaxf(fabsf(d[i].x), fabsf(d[i].y)) > 0.5f - 1.0f / 16384.0f;
     }
     if (near_tie) {
@@ -224,16 +227,18 @@ __device__ __forceinline__ void codes8(const float (&v)[8], float z, float s, fl
 }
 
 // Lane-held octet of 8 b-bit codes: code i at bits [b*i, b*i+b) of (lo, hi).
+// The fields are disjoint and q < 2^b, so adding a code equals OR-ing it in
+// (and is one shift-add).
 template <int BITS>
 struct Octet {
     uint32_t lo = 0, hi = 0;
     __device__ __forceinline__ void put(int i, uint32_t q) {
         const int b = BITS * i;
         if (b < 32) {
-            lo |= q << b;
-            if (b + BITS > 32) hi |= q >> (32 - b);
+            lo += q << b;
+            if (b + BITS > 32) hi += q >> (32 - b);
         } else {
-            hi |= q << (b - 32);
+            hi += q << (b - 32);
         }
     }
     __device__ __forceinline__ uint8_t byte(int i) const {
@@ -402,11 +407,9 @@ quantize_kernel(const void *__restrict__ w, int dtype, uint8_t *__restrict__ pac
 #pragma unroll
                 for (int h = 0; h < kOct; ++h) {
                     uint32_t q[8];
-                    codes8(block(h).v, z, s, inv_s, q);
-                    // The mask changes no valid code; it keeps a NaN weight's
-                    // code (0, as before) from spilling into its neighbours.
+                    codes8(block(h).v, z, s, inv_s, (1u << BITS) - 1u, q);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) o[h].put(i, q[i] & ((1u << BITS) - 1u));
+                    for (int i = 0; i < 8; ++i) o[h].put(i, q[i]);
                 }
             }
             uint8_t *dst = packed + n * row_bytes + (int64_t)(k / 8) * BITS;
